@@ -1,0 +1,369 @@
+"""Throughput of the DSA layer (fused Lightning Indexer → Top-K → sparse MLA attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode] [--impl ours|reference]
+
+One step = one dsa_fused_forward over one batch of the workload (all of the
+path's steps: scoring, head weighting, Top-K, gather, attention), inputs
+resident in HBM.  L2 is flushed (a 256 MB write) before every timed step,
+outside the step's CUDA events.  Prints one JSON line on rank 0.
+
+Under torchrun (N > 1) every rank runs its own batch (seed offset by rank; the
+sequences are independent, so no collective is on the data path): weak scaling,
+value = all ranks' tokens ÷ the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the only other arm this path has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DSA tokens/sec (decode, prefill) on 1 GB300; % HBM and tensor-core roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def describe(cfg) -> str:
+    ql, kl = cfg.q_lens, cfg.k_lens
+    lens = f"L={kl[0]}" if len(set(kl)) == 1 else f"L~[{min(kl)},{max(kl)}] (sum {sum(kl)})"
+    return (f"{cfg.name}: B={cfg.num_seqs} T={sum(ql)} {lens} H_I={cfg.h_idx} d_I={cfg.d_idx} "
+            f"H={cfg.h} d_c={cfg.d_c} d_rope={cfg.d_rope} top_k={cfg.top_k} "
+            f"idx={cfg.idx_dtype} kv={cfg.kv_dtype}")
+
+
+def positions(cfg):
+    for T, L in zip(cfg.q_lens, cfg.k_lens):
+        for i in range(T):
+            yield L - T + i
+
+
+def work_model(cfg):
+    """Algorithmic bytes and flops of each stage (what the method must move/compute)."""
+    es_i = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.idx_dtype]
+    es_kv = {"f32": 4, "bf16": 2}[cfg.kv_dtype]
+    es_o = {"f32": 4, "bf16": 2}[cfg.out_dtype]
+    TQ, TK, D = cfg.total_q, cfg.total_k, cfg.d
+    pairs = sum(p + 1 for p in positions(cfg))               # causal (query, key) pairs
+    sel = sum(min(cfg.top_k, p + 1) for p in positions(cfg))  # selected (query, row) pairs
+    scales = (TK * 4 + TQ * cfg.h_idx * 4) if cfg.idx_dtype == "e4m3" else 0
+    idx_b = TQ * cfg.top_k * 4
+    indexer_bytes = TK * cfg.d_idx * es_i + TQ * cfg.h_idx * (cfg.d_idx * es_i + 4) + scales + idx_b
+    sfa_bytes = TQ * cfg.h * D * es_kv + sel * D * es_kv + idx_b + TQ * cfg.h * (cfg.d_c * es_o + 4)
+    return {
+        "indexer": {"bytes": indexer_bytes, "flops": 2 * cfg.h_idx * cfg.d_idx * pairs},
+        "sfa": {"bytes": sfa_bytes, "flops": 2 * cfg.h * (D + cfg.d_c) * sel},
+        "pairs": pairs, "selected": sel,
+    }
+
+
+# Which stage each library kernel belongs to (for the roofline of the dominant kernel).
+KERNEL_STAGE = {
+    "indexer_scores_simt": "indexer", "topk_rows": "topk", "sfa_simt": "sfa",
+}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.3)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_baseline(case, budget_s=(10.0, 30.0), rows=None):
+    """Time the fp64 oracle on whole passes over `rows` until >= budget_s[0] seconds."""
+    from oracle import dsa_oracle as O
+    p = O.problem_from_case(case)
+    rows = list(range(case.cfg.total_q)) if rows is None else list(rows)
+    done, t0 = 0, time.perf_counter()
+    passes = 0
+    while True:
+        for t in rows:
+            p.forward_row(t)
+            done += 1
+            if time.perf_counter() - t0 > budget_s[1]:
+                break
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s[0] or el > budget_s[1]:
+            break
+    return done, el, passes
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, cfg, case, rank):
+    """The oracle arm: each step = the oracle over a bounded sample of query rows."""
+    if rank != 0:
+        return
+    from oracle import dsa_oracle as O
+    p = O.problem_from_case(case)
+    n_sample = max(1, min(cfg.total_q, args.ref_rows))
+    rows = list(range(n_sample))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for t in rows:
+            p.forward_row(t)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    el = sum(times)
+    value = n_sample * len(times) / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(cfg), "sample_rows_per_step": n_sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"first {n_sample} query rows of the workload per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "tiny_prefill", "prefill_8k", "prefill_64k", "fp8_decode"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=8, help="oracle rows per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        os.environ.setdefault("OPENBLAS_NUM_THREADS", str(cores()))
+
+    import torch
+    import torch.distributed as dist
+
+    from sparse_attention_lightning_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+
+    cfg = W.workload(args.workload)
+    seed = W.WORKLOAD_SEEDS[args.workload] + 1000 * rank
+    if args.impl == "reference":
+        if rank == 0:
+            case = W.make_case(cfg, seed)
+            run_reference(args, cfg, case, rank)
+        return
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import sparse_attention_lightning_gb300 as dsa
+    dsa.lib()
+
+    case = W.make_case(cfg, seed)
+    d = {k: v.to(dev) for k, v in case.tensors().items()}
+    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"])
+    ws = dsa.Workspace(dev, P.workspace_size(5))
+    out = torch.empty(cfg.total_q, cfg.h, cfg.d_c, dtype=torch.bfloat16 if cfg.out_dtype == "bf16"
+                      else torch.float32, device=dev)
+    lse = torch.empty(cfg.total_q, cfg.h, dtype=torch.float32, device=dev)
+    idx = torch.empty(cfg.total_q, cfg.top_k, dtype=torch.int32, device=dev)
+
+    def step():
+        dsa.fused_forward(P, d["q_idx"], d["k_idx"], d["w"], d["q"], d["kv"], d.get("q_scale"),
+                          d.get("k_scale"), out=out, lse=lse, idx=idx, ws=ws)
+
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    ws.clear_status()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    flags = ws.status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with dsa.trace(capacity=64 * args.steps) as tr:
+            for i in range(args.steps):
+                flush.zero_()
+                evs[i][0].record()
+                step()
+                evs[i][1].record()
+            torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    total_ms = float(t_max.item())
+    tokens = cfg.total_q * args.steps * world
+    value = tokens / (total_ms / 1e3)
+
+    # per-kernel times (CUDA events around each launch, on its stream)
+    per_kernel = {}
+    for name, ms in tr.records:
+        per_kernel.setdefault(name, []).append(ms)
+    model = work_model(cfg)
+    peaks, peak_src = load_peaks()
+    dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
+    dom_ms = statistics.mean(per_kernel[dom])
+    stage = KERNEL_STAGE.get(dom, dom)
+    decode_like = max(cfg.q_lens) == 1
+    if decode_like or stage == "topk":
+        alg = model[stage]["bytes"] if stage in model else cfg.total_q * cfg.top_k * 4
+        achieved = alg / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": dom,
+                "algorithmic_bytes_per_launch": alg, "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        alg = model[stage]["flops"]
+        achieved = alg / (dom_ms / 1e3) / 1e12
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                "frac": achieved / pk, "traffic": None, "kernel": dom,
+                "algorithmic_flops_per_launch": alg, "peak_source": f"{peak_src} bf16_tflops"}
+    roof["kernel_ms_mean"] = dom_ms
+    kernels = {k: {"launches": len(v), "ms_mean": statistics.mean(v),
+                   "share": sum(v) / sum(sum(x) for x in per_kernel.values())}
+               for k, v in per_kernel.items()}
+
+    # end to end through the public API: per-step inputs from pinned host memory, result back
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: case.tensors()[k].pin_memory() for k in ("q_idx", "w", "q", "q_scale")
+                   if k in case.tensors()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = out_h.numel() * out_h.element_size()
+        e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            if i >= args.warmup:
+                e_evs[i - args.warmup][0].record()
+            for k, v in host_in.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            if i >= args.warmup:
+                e_evs[i - args.warmup][1].record()
+            torch.cuda.synchronize()
+        e_ms = sum(a.elapsed_time(b) for a, b in e_evs)
+        e_t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(e_t, op=dist.ReduceOp.MAX)
+        e2e = {"value": tokens / (float(e_t.item()) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "per-step query-side inputs (q_idx, w, q) host->device and out "
+                       "device->host; K/latent caches are device-resident state"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, el, passes = oracle_baseline(case)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"{n} query rows of this workload ({passes} pass(es) over its "
+                         f"{cfg.total_q} rows), fp64 numpy, BLAS threads = default",
+               "seconds": el}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.kv_dtype if cfg.idx_dtype != "e4m3" else "e4m3+bf16",
+            "data": "synthetic (seeded N(0,1/sqrt(d)) values, w~U(0,1))",
+            "config": {"workload": describe(cfg), "tokens_per_step_per_gpu": cfg.total_q,
+                       "l2": "flushed (256 MB write) before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,
+            "clocks": clk.summary(), "e2e": e2e, "gpu_launches": len(tr.records),
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

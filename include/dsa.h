@@ -1,0 +1,221 @@
+/*
+ * dsa.h — C ABI of libdsa.so, the GB300 (sm_103a) DSA hot path.
+ *
+ * DSA ("dynamic sparse attention") is the sparse-attention layer of a hybrid
+ * MLA-based model.  A lightweight Lightning Indexer scores every historical
+ * position of a query, keeps the Top-K positions, and Sparse Flash Attention
+ * (SFA) attends over the MLA latent KV rows at just those positions
+ * ("Day0 Inference Adaptation and Performance Optimization for New-Architecture
+ * LLMs", §2.2 The Sparse Attention Path and §4.1 Indexer Fusion; "Day0 Inference
+ * Adaptation and Performance Optimization for a New Architecture Domestic Large
+ * Language Model on Ascend", §2 and §4).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Return value.  Every call returns a dsa_status code (0 = DSA_OK).  No C++
+ *   exception crosses the ABI.  dsa_last_error() gives a message for the last
+ *   failing call of the calling thread.
+ * Pointers.  Every tensor pointer is caller-owned DEVICE memory (cudaMalloc or
+ *   torch), 16-byte aligned.  The library never allocates, frees or retains
+ *   them.  Tensors are dense, row-major, packed along tokens (no padding
+ *   between sequences).
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Calls only enqueue work; argument checks are synchronous and a
+ *   failing check launches nothing.
+ * Workspace.  Every call takes a caller-owned device workspace of at least
+ *   dsa_workspace_size() bytes.  Its first 256 bytes hold a device status word:
+ *   kernels OR DSA_FLAG_* bits into it when they detect bad data (an index out
+ *   of range, inconsistent cu_q/cu_k) or give up a bounded wait.  The word is
+ *   sticky: clear it with dsa_clear_status() (or zero the workspace once) and
+ *   read it with dsa_read_status().  The rest is scratch owned by the call
+ *   while it runs; calls sharing one workspace must be stream-ordered.
+ * Sequences.  Query rows and key rows are packed: sequence b owns query rows
+ *   cu_q[b] .. cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1, with
+ *   T_b = cu_q[b+1]-cu_q[b] <= L_b = cu_k[b+1]-cu_k[b].  The queries of a
+ *   sequence are its last T_b tokens: query i of sequence b is at position
+ *   pos = L_b - T_b + i and sees keys 0..pos of its own sequence (causal,
+ *   inclusive; index computation is causal, "… New-Architecture LLMs" §6.2).
+ *   Prefill has T_b = L_b (pos = i); decode has T_b = 1 (pos = L_b - 1).
+ *   Positions written to / read from `idx` are local to the sequence.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+/* Return codes. */
+enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, inconsistent descriptor */
+  DSA_ERR_UNSUPPORTED = 2,  /* a valid combination this build has no kernel for */
+  DSA_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed */
+  DSA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than dsa_workspace_size() */
+  DSA_ERR_TIMEOUT = 5       /* dsa_read_status saw DSA_FLAG_TIMEOUT */
+};
+
+/* Element types. */
+enum dsa_dtype {
+  DSA_F32 = 0,       /* IEEE binary32 */
+  DSA_BF16 = 1,      /* bfloat16 */
+  DSA_FP8_E4M3 = 2   /* OCP FP8 E4M3 ("fn": no infinities), with fp32 scales */
+};
+
+/* Device status flags (bits of the workspace status word). */
+#define DSA_FLAG_BAD_INDEX 0x1u  /* SFA met an index outside [0, pos]; that entry was skipped */
+#define DSA_FLAG_BAD_SEQS  0x2u  /* cu_q/cu_k inconsistent with the descriptor; rows were skipped */
+#define DSA_FLAG_TIMEOUT   0x4u  /* a bounded on-device wait gave up; outputs are not valid */
+
+/* Operations, for dsa_workspace_size(). */
+enum dsa_op {
+  DSA_OP_INDEXER_SCORES = 1,
+  DSA_OP_TOPK = 2,
+  DSA_OP_FUSED_INDEXER = 3,
+  DSA_OP_SPARSE_MLA_ATTN = 4,
+  DSA_OP_FUSED_FORWARD = 5
+};
+
+/* Shape, types and sequence layout of one DSA problem. */
+typedef struct dsa_problem {
+  int32_t num_seqs;    /* B >= 1 */
+  int32_t total_q;     /* ΣT_b >= 0: packed query rows */
+  int32_t total_k;     /* ΣL_b >= 1: packed key rows */
+  int32_t max_q_len;   /* max_b T_b (an upper bound is fine) */
+  int32_t max_k_len;   /* max_b L_b (an upper bound is fine) */
+  int32_t h_idx;       /* H_I: indexer heads */
+  int32_t d_idx;       /* d_I: indexer head width */
+  int32_t h;           /* H: MLA query heads (all share one latent row per key) */
+  int32_t d_c;         /* latent width = value width */
+  int32_t d_rope;      /* rope width; a latent row has D = d_c + d_rope columns */
+  int32_t top_k;       /* k: positions kept per query */
+  int32_t idx_dtype;   /* dsa_dtype of q_idx and k_idx (F32, BF16 or FP8_E4M3) */
+  int32_t kv_dtype;    /* dsa_dtype of q and kv (F32 or BF16) */
+  int32_t out_dtype;   /* dsa_dtype of out (F32 or BF16) */
+  float sm_scale;      /* softmax scale; 0 selects 1/sqrt(D) */
+  const int32_t* cu_q; /* device int32 [B+1], cu_q[0] = 0, cu_q[B] = total_q */
+  const int32_t* cu_k; /* device int32 [B+1], cu_k[0] = 0, cu_k[B] = total_k */
+} dsa_problem;
+
+/* Limits of this build: 1 <= h_idx <= 128, d_idx in {16..256, multiple of 16},
+ * 1 <= h <= 128, d_c in {16..1024, multiple of 16}, d_rope in {0..256, multiple
+ * of 16}, 1 <= top_k <= 2048, max_k_len <= 2^30.  Outside them a call returns
+ * DSA_ERR_UNSUPPORTED. */
+
+/* Bytes of workspace `op` needs for problem `p` (always >= 256). */
+int dsa_workspace_size(const dsa_problem* p, int op, size_t* bytes);
+
+/*
+ * Lightning-Indexer relevance scores, materialised (for checking and
+ * debugging; the fused calls below never write them to memory).
+ *   scores[t, s] = Σ_j w[t,j] · ReLU(q_idx[t,j,:] · k_idx[s,:])   for s <= pos(t)
+ *   scores[t, s] = -inf                                          for pos(t) < s < ld
+ * ("… New-Architecture LLMs" §4.1: batched dot of the indexer query with the K
+ * cache, then a weighted sum over heads; §2.2: each historical position gets a
+ * relevance score.)
+ * q_idx  [total_q, h_idx, d_idx] idx_dtype
+ * k_idx  [total_k, d_idx]        idx_dtype
+ * w      [total_q, h_idx]        f32 head weights
+ * q_scale [total_q, h_idx] f32, k_scale [total_k] f32: dequantisation scales,
+ *        required (and > 0) for FP8_E4M3, ignored (may be NULL) otherwise:
+ *        q = code·q_scale[t,j], k = code·k_scale[s].
+ * scores [total_q, ld] f32, ld >= max_k_len.
+ */
+int dsa_indexer_scores(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                       const float* w, const float* q_scale, const float* k_scale,
+                       float* scores, int64_t ld, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Causal Top-K of materialised scores (Top-K selection of the indexer,
+ * "… New-Architecture LLMs" §4.1).  For each query row t, idx[t, 0..n-1]
+ * (n = min(top_k, pos+1)) receives the positions of the n largest
+ * scores[t, 0..pos], in ascending position order; among equal scores the
+ * smaller positions are kept.  idx[t, n..top_k-1] = -1.
+ * scores [total_q, ld] f32 (only columns 0..pos(t) are read)
+ * idx    [total_q, top_k] int32
+ * vals   [total_q, top_k] f32 or NULL: the selected scores (-inf in padding).
+ */
+int dsa_topk(const dsa_problem* p, const float* scores, int64_t ld, int32_t* idx, float* vals,
+             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The fused Lightning Indexer: scoring, head weighting and Top-K in one pass
+ * over the K cache, writing only the selected positions ("… New-Architecture
+ * LLMs" §4.1 fused_indexer(q_idx, k_cache, head_weights, top_k); "Optimizing
+ * LLM Inference for New Architectures", §3: only the final Top-K indices leave
+ * the operator).  Arguments and results are those of dsa_indexer_scores
+ * followed by dsa_topk.
+ */
+int dsa_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                      const float* w, const float* q_scale, const float* k_scale,
+                      int32_t* idx, float* vals, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Sparse Flash Attention over the MLA latent cache at the selected positions
+ * ("… New-Architecture LLMs" §2.2 and §4.1: gather the selected KV rows and
+ * attend over that subset; "… on Ascend" §4: SFA reads the KV cache at the
+ * position set the indexer outputs).  For query row t and head h, over the
+ * valid entries i of idx[t, :]:
+ *   S_i = sm_scale · q[t,h,:] · kv[cu_k[b] + idx[t,i], :]        (all D columns)
+ *   out[t,h,:] = Σ_i softmax(S)_i · kv[cu_k[b] + idx[t,i], 0:d_c]
+ *   lse[t,h]   = log Σ_i exp(S_i)                                 (natural log)
+ * q   [total_q, h, D] kv_dtype;  kv [total_k, D] kv_dtype (D = d_c + d_rope)
+ * idx [total_q, top_k] int32: -1 entries are skipped; an entry outside
+ *     [0, pos(t)] sets DSA_FLAG_BAD_INDEX and is skipped; order is free;
+ *     a repeated entry counts as often as it appears.
+ * out [total_q, h, d_c] out_dtype; lse [total_q, h] f32 or NULL.
+ * A row with no valid entry gets out = 0 and lse = -inf.
+ */
+int dsa_sparse_mla_attn(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx,
+                        void* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole DSA layer: dsa_fused_indexer then dsa_sparse_mla_attn on the same
+ * stream ("… on Ascend" §4: the fused indexer's selected positions feed SFA).
+ * idx_out [total_q, top_k] int32 and vals_out [total_q, top_k] f32 are optional
+ * (NULL: kept in the workspace only).
+ */
+int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                      const float* w, const float* q_scale, const float* k_scale,
+                      const void* q, const void* kv, void* out, float* lse,
+                      int32_t* idx_out, float* vals_out, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* Zero the workspace status word (enqueued on `stream`). */
+int dsa_clear_status(void* ws, void* stream);
+
+/* Synchronise `stream`, then copy the workspace status word into *flags.
+ * Returns DSA_ERR_TIMEOUT if DSA_FLAG_TIMEOUT is set, DSA_OK otherwise. */
+int dsa_read_status(const void* ws, void* stream, uint32_t* flags);
+
+/* Message of a dsa_status code (static storage). */
+const char* dsa_status_str(int status);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* dsa_last_error(void);
+
+/* DSA_ABI_VERSION of the loaded library. */
+int dsa_abi_version(void);
+
+/*
+ * Launch tracing.  Between dsa_trace_begin(capacity) and dsa_trace_end(), every
+ * kernel the library launches is bracketed by a pair of CUDA events recorded on
+ * its stream (at most `capacity` launches are kept).  dsa_trace_get() returns
+ * the kernel name and the elapsed milliseconds of launch i (it waits for that
+ * launch's end event).  dsa_trace_count() gives the number recorded.
+ */
+int dsa_trace_begin(int capacity);
+int dsa_trace_end(void);
+int dsa_trace_count(void);
+int dsa_trace_get(int i, char* name, int name_len, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

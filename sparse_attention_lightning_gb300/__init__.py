@@ -1,0 +1,289 @@
+"""GB300 (sm_103a) DSA hot path: Lightning Indexer → Top-K → sparse MLA attention.
+
+A thin binding over libdsa.so (include/dsa.h).  Functions take CUDA tensors,
+check their dtypes and shapes, and pass raw pointers plus the current CUDA
+stream to the library; every step of the computation runs in the library's
+kernels.  There is no CPU or framework fallback: if the library is missing,
+calls raise.
+
+Names follow the C ABI: indexer_scores, topk, fused_indexer, sparse_mla_attn,
+fused_forward.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import _abi
+from ._abi import DsaError, lib  # noqa: F401
+
+__all__ = ["Problem", "Workspace", "indexer_scores", "topk", "fused_indexer", "sparse_mla_attn",
+           "fused_forward", "DsaError", "lib", "trace"]
+
+_DT = {torch.float32: _abi.DSA_F32, torch.bfloat16: _abi.DSA_BF16,
+       torch.uint8: _abi.DSA_FP8_E4M3, torch.float8_e4m3fn: _abi.DSA_FP8_E4M3}
+_NAME_DT = {"f32": _abi.DSA_F32, "bf16": _abi.DSA_BF16, "e4m3": _abi.DSA_FP8_E4M3}
+_TORCH_OUT = {_abi.DSA_F32: torch.float32, _abi.DSA_BF16: torch.bfloat16}
+
+
+def _dt(x) -> int:
+    if isinstance(x, str):
+        return _NAME_DT[x]
+    if isinstance(x, int):
+        return x
+    return _DT[x]
+
+
+class Problem:
+    """Sizes, dtypes and device sequence offsets of one DSA problem (dsa_problem)."""
+
+    def __init__(self, cu_q: torch.Tensor, cu_k: torch.Tensor, *, q_lens: Sequence[int],
+                 k_lens: Sequence[int], h_idx: int, d_idx: int, h: int, d_c: int, d_rope: int,
+                 top_k: int, idx_dtype, kv_dtype, out_dtype=None, sm_scale: float = 0.0):
+        if not (cu_q.is_cuda and cu_k.is_cuda) or cu_q.dtype != torch.int32 \
+                or cu_k.dtype != torch.int32:
+            raise ValueError("cu_q/cu_k must be int32 CUDA tensors")
+        self.cu_q, self.cu_k = cu_q.contiguous(), cu_k.contiguous()
+        self.q_lens, self.k_lens = list(q_lens), list(k_lens)
+        self.h_idx, self.d_idx, self.h, self.d_c, self.d_rope = h_idx, d_idx, h, d_c, d_rope
+        self.top_k = top_k
+        self.idx_dtype, self.kv_dtype = _dt(idx_dtype), _dt(kv_dtype)
+        self.out_dtype = _dt(out_dtype) if out_dtype is not None else self.kv_dtype
+        self.sm_scale = float(sm_scale)
+        self.c = _abi.DsaProblem(
+            len(self.q_lens), sum(self.q_lens), sum(self.k_lens), max(self.q_lens, default=0),
+            max(self.k_lens), h_idx, d_idx, h, d_c, d_rope, top_k, self.idx_dtype, self.kv_dtype,
+            self.out_dtype, self.sm_scale, self.cu_q.data_ptr(), self.cu_k.data_ptr())
+
+    @classmethod
+    def from_config(cls, cfg, cu_q: torch.Tensor, cu_k: torch.Tensor, sm_scale: float = 0.0):
+        return cls(cu_q, cu_k, q_lens=cfg.q_lens, k_lens=cfg.k_lens, h_idx=cfg.h_idx,
+                   d_idx=cfg.d_idx, h=cfg.h, d_c=cfg.d_c, d_rope=cfg.d_rope, top_k=cfg.top_k,
+                   idx_dtype=cfg.idx_dtype, kv_dtype=cfg.kv_dtype, out_dtype=cfg.out_dtype,
+                   sm_scale=sm_scale)
+
+    @property
+    def total_q(self) -> int:
+        return self.c.total_q
+
+    @property
+    def total_k(self) -> int:
+        return self.c.total_k
+
+    @property
+    def max_k_len(self) -> int:
+        return self.c.max_k_len
+
+    @property
+    def d(self) -> int:
+        return self.d_c + self.d_rope
+
+    @property
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale > 0 else 1.0 / math.sqrt(self.d)
+
+    def workspace_size(self, op: int) -> int:
+        n = ctypes.c_size_t(0)
+        _abi.check(lib().dsa_workspace_size(ctypes.byref(self.c), op, ctypes.byref(n)))
+        return n.value
+
+
+class Workspace:
+    """Caller-owned device scratch with the status word in its first 256 bytes."""
+
+    def __init__(self, device=None, nbytes: int = 256):
+        self.device = torch.device(device or "cuda")
+        self.buf = torch.zeros(max(256, nbytes), dtype=torch.uint8, device=self.device)
+
+    def ensure(self, nbytes: int) -> "Workspace":
+        if self.buf.numel() < nbytes:
+            flags = self.buf[:256].clone()
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+            self.buf[:256].copy_(flags)
+        return self
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+    def clear_status(self) -> None:
+        _abi.check(lib().dsa_clear_status(self.ptr, _stream(self.device)))
+
+    def status(self) -> int:
+        """Synchronise the current stream and return the device status flags."""
+        f = ctypes.c_uint32(0)
+        rc = lib().dsa_read_status(self.ptr, _stream(self.device), ctypes.byref(f))
+        if rc not in (_abi.DSA_OK, _abi.DSA_ERR_TIMEOUT):
+            _abi.check(rc)
+        return f.value
+
+
+_default_ws = {}
+
+
+def _workspace(ws: Optional[Workspace], device, nbytes: int) -> Workspace:
+    if ws is None:
+        key = torch.device(device).index
+        ws = _default_ws.get(key)
+        if ws is None:
+            ws = _default_ws[key] = Workspace(device, nbytes)
+    return ws.ensure(nbytes)
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: Optional[torch.Tensor], name: str, dtype_code: Optional[int], shape: Tuple[int, ...],
+          optional: bool = False) -> None:
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype_code is not None and _DT.get(t.dtype) != dtype_code:
+        raise ValueError(f"{name} has dtype {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_indexer(P: Problem, q_idx, k_idx, w, q_scale, k_scale):
+    _need(q_idx, "q_idx", P.idx_dtype, (P.total_q, P.h_idx, P.d_idx))
+    _need(k_idx, "k_idx", P.idx_dtype, (P.total_k, P.d_idx))
+    _need(w, "w", _abi.DSA_F32, (P.total_q, P.h_idx))
+    fp8 = P.idx_dtype == _abi.DSA_FP8_E4M3
+    _need(q_scale, "q_scale", _abi.DSA_F32, (P.total_q, P.h_idx), optional=not fp8)
+    _need(k_scale, "k_scale", _abi.DSA_F32, (P.total_k,), optional=not fp8)
+
+
+def _idx_out(P: Problem, idx, vals, device, want_vals: bool):
+    if idx is None:
+        idx = torch.empty(P.total_q, P.top_k, dtype=torch.int32, device=device)
+    _need(idx, "idx", None, (P.total_q, P.top_k))
+    if vals is None and want_vals:
+        vals = torch.empty(P.total_q, P.top_k, dtype=torch.float32, device=device)
+    _need(vals, "vals", _abi.DSA_F32, (P.total_q, P.top_k), optional=True)
+    return idx, vals
+
+
+def indexer_scores(P: Problem, q_idx, k_idx, w, q_scale=None, k_scale=None, scores=None,
+                   ws: Optional[Workspace] = None) -> torch.Tensor:
+    """scores[ΣT, max_k_len] (fp32, -inf past each query's position)."""
+    _check_indexer(P, q_idx, k_idx, w, q_scale, k_scale)
+    dev = k_idx.device
+    if scores is None:
+        scores = torch.empty(P.total_q, P.max_k_len, dtype=torch.float32, device=dev)
+    _need(scores, "scores", _abi.DSA_F32, (P.total_q, scores.shape[1]))
+    ws = _workspace(ws, dev, P.workspace_size(_abi.OP_INDEXER_SCORES))
+    _abi.check(lib().dsa_indexer_scores(
+        ctypes.byref(P.c), q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), _ptr(q_scale),
+        _ptr(k_scale), scores.data_ptr(), scores.shape[1], ws.ptr, ws.nbytes, _stream(dev)))
+    return scores
+
+
+def topk(P: Problem, scores: torch.Tensor, idx=None, vals=None, want_vals: bool = False,
+         ws: Optional[Workspace] = None):
+    """(idx[ΣT, top_k] int32 ascending positions, -1 padded; vals or None)."""
+    _need(scores, "scores", _abi.DSA_F32, (P.total_q, scores.shape[1]))
+    dev = scores.device
+    idx, vals = _idx_out(P, idx, vals, dev, want_vals)
+    ws = _workspace(ws, dev, P.workspace_size(_abi.OP_TOPK))
+    _abi.check(lib().dsa_topk(ctypes.byref(P.c), scores.data_ptr(), scores.shape[1],
+                              idx.data_ptr(), _ptr(vals), ws.ptr, ws.nbytes, _stream(dev)))
+    return idx, vals
+
+
+def fused_indexer(P: Problem, q_idx, k_idx, w, q_scale=None, k_scale=None, idx=None, vals=None,
+                  want_vals: bool = False, ws: Optional[Workspace] = None):
+    """Scoring + head weighting + Top-K in one call: (idx, vals or None)."""
+    _check_indexer(P, q_idx, k_idx, w, q_scale, k_scale)
+    dev = k_idx.device
+    idx, vals = _idx_out(P, idx, vals, dev, want_vals)
+    ws = _workspace(ws, dev, P.workspace_size(_abi.OP_FUSED_INDEXER))
+    _abi.check(lib().dsa_fused_indexer(
+        ctypes.byref(P.c), q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), _ptr(q_scale),
+        _ptr(k_scale), idx.data_ptr(), _ptr(vals), ws.ptr, ws.nbytes, _stream(dev)))
+    return idx, vals
+
+
+def _attn_out(P: Problem, out, lse, device, want_lse: bool):
+    if out is None:
+        out = torch.empty(P.total_q, P.h, P.d_c, dtype=_TORCH_OUT[P.out_dtype], device=device)
+    _need(out, "out", P.out_dtype, (P.total_q, P.h, P.d_c))
+    if lse is None and want_lse:
+        lse = torch.empty(P.total_q, P.h, dtype=torch.float32, device=device)
+    _need(lse, "lse", _abi.DSA_F32, (P.total_q, P.h), optional=True)
+    return out, lse
+
+
+def sparse_mla_attn(P: Problem, q, kv, idx, out=None, lse=None, want_lse: bool = True,
+                    ws: Optional[Workspace] = None):
+    """Sparse attention over the latent rows idx selects: (out[ΣT, H, d_c], lse or None)."""
+    _need(q, "q", P.kv_dtype, (P.total_q, P.h, P.d))
+    _need(kv, "kv", P.kv_dtype, (P.total_k, P.d))
+    _need(idx, "idx", None, (P.total_q, P.top_k))
+    dev = kv.device
+    out, lse = _attn_out(P, out, lse, dev, want_lse)
+    ws = _workspace(ws, dev, P.workspace_size(_abi.OP_SPARSE_MLA_ATTN))
+    _abi.check(lib().dsa_sparse_mla_attn(ctypes.byref(P.c), q.data_ptr(), kv.data_ptr(),
+                                         idx.data_ptr(), out.data_ptr(), _ptr(lse), ws.ptr,
+                                         ws.nbytes, _stream(dev)))
+    return out, lse
+
+
+def fused_forward(P: Problem, q_idx, k_idx, w, q, kv, q_scale=None, k_scale=None, out=None,
+                  lse=None, idx=None, vals=None, want_lse: bool = True, want_idx: bool = True,
+                  want_vals: bool = False, ws: Optional[Workspace] = None):
+    """The DSA layer: fused indexer then sparse attention → (out, lse, idx, vals)."""
+    _check_indexer(P, q_idx, k_idx, w, q_scale, k_scale)
+    _need(q, "q", P.kv_dtype, (P.total_q, P.h, P.d))
+    _need(kv, "kv", P.kv_dtype, (P.total_k, P.d))
+    dev = kv.device
+    out, lse = _attn_out(P, out, lse, dev, want_lse)
+    if want_idx or idx is not None:
+        idx, vals = _idx_out(P, idx, vals, dev, want_vals)
+    elif want_vals or vals is not None:
+        raise ValueError("vals needs idx")
+    ws = _workspace(ws, dev, P.workspace_size(_abi.OP_FUSED_FORWARD))
+    _abi.check(lib().dsa_fused_forward(
+        ctypes.byref(P.c), q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), _ptr(q_scale),
+        _ptr(k_scale), q.data_ptr(), kv.data_ptr(), out.data_ptr(), _ptr(lse), _ptr(idx),
+        _ptr(vals), ws.ptr, ws.nbytes, _stream(dev)))
+    return out, lse, idx, vals
+
+
+class trace:
+    """Context manager recording per-launch CUDA-event times of the library's kernels."""
+
+    def __init__(self, capacity: int = 4096):
+        self.capacity = capacity
+        self.records = []
+
+    def __enter__(self):
+        _abi.check(lib().dsa_trace_begin(self.capacity))
+        return self
+
+    def __exit__(self, *exc):
+        _abi.check(lib().dsa_trace_end())
+        n = lib().dsa_trace_count()
+        name = ctypes.create_string_buffer(128)
+        ms = ctypes.c_float(0)
+        self.records = []
+        for i in range(n):
+            _abi.check(lib().dsa_trace_get(i, name, 128, ctypes.byref(ms)))
+            self.records.append((name.value.decode(), ms.value))
+        return False

@@ -1,0 +1,388 @@
+// C ABI of libdsa.so: argument checks, workspace carving, kernel dispatch,
+// status word, error strings and launch tracing.  See include/dsa.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "dsa_internal.cuh"
+
+namespace dsa {
+
+// ----------------------------------------------------------------------------
+// Errors.
+static thread_local std::string g_last_error;
+
+int set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return DSA_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Launch tracing: an event pair around each launch while enabled.
+namespace {
+struct TraceRec {
+  std::string name;
+  cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+int g_trace_cap = 0;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+int g_trace_open = -1;  // record awaiting its end event
+}  // namespace
+
+void trace_pre(const char* name, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on || (int)g_trace.size() >= g_trace_cap) return;
+  const size_t i = g_trace.size();
+  TraceRec r{name, g_event_pool[2 * i], g_event_pool[2 * i + 1]};
+  cudaEventRecord(r.a, s);
+  g_trace.push_back(r);
+  g_trace_open = (int)i;
+}
+
+void trace_post(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_trace_open < 0) return;
+  cudaEventRecord(g_trace[g_trace_open].b, s);
+  g_trace_open = -1;
+}
+
+// ----------------------------------------------------------------------------
+// Descriptor checks.
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_ptr(const void* p, const char* name, bool nullable = false) {
+  if (!p) {
+    if (nullable) return DSA_OK;
+    return set_error(DSA_ERR_INVALID_ARG, "%s is NULL", name);
+  }
+  if (!aligned16(p)) return set_error(DSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return DSA_OK;
+}
+
+size_t dtype_size(int dt) { return dt == DSA_F32 ? 4 : dt == DSA_BF16 ? 2 : 1; }
+
+int check_problem(const dsa_problem* p, bool need_indexer, bool need_attn) {
+  if (!p) return set_error(DSA_ERR_INVALID_ARG, "problem descriptor is NULL");
+  if (p->num_seqs < 1) return set_error(DSA_ERR_INVALID_ARG, "num_seqs = %d", p->num_seqs);
+  if (p->total_q < 0 || p->total_k < 1)
+    return set_error(DSA_ERR_INVALID_ARG, "total_q = %d, total_k = %d", p->total_q, p->total_k);
+  if (p->max_k_len < 1 || p->max_k_len > p->total_k || p->max_q_len < 0 ||
+      p->max_q_len > p->max_k_len)
+    return set_error(DSA_ERR_INVALID_ARG, "max_q_len = %d, max_k_len = %d", p->max_q_len,
+                     p->max_k_len);
+  if (p->max_k_len > (1 << 30)) return set_error(DSA_ERR_UNSUPPORTED, "max_k_len > 2^30");
+  if (p->top_k < 1 || p->top_k > 2048)
+    return set_error(DSA_ERR_UNSUPPORTED, "top_k = %d (supported 1..2048)", p->top_k);
+  if (!p->cu_q || !p->cu_k) return set_error(DSA_ERR_INVALID_ARG, "cu_q/cu_k is NULL");
+  if (need_indexer) {
+    if (p->h_idx < 1 || p->h_idx > 128)
+      return set_error(DSA_ERR_UNSUPPORTED, "h_idx = %d (supported 1..128)", p->h_idx);
+    if (p->d_idx < 16 || p->d_idx > 256 || p->d_idx % 16)
+      return set_error(DSA_ERR_UNSUPPORTED, "d_idx = %d (supported 16..256, multiple of 16)",
+                       p->d_idx);
+    if (p->idx_dtype != DSA_F32 && p->idx_dtype != DSA_BF16 && p->idx_dtype != DSA_FP8_E4M3)
+      return set_error(DSA_ERR_INVALID_ARG, "idx_dtype = %d", p->idx_dtype);
+  }
+  if (need_attn) {
+    if (p->h < 1 || p->h > 128) return set_error(DSA_ERR_UNSUPPORTED, "h = %d (1..128)", p->h);
+    if (p->d_c < 16 || p->d_c > 1024 || p->d_c % 16)
+      return set_error(DSA_ERR_UNSUPPORTED, "d_c = %d (16..1024, multiple of 16)", p->d_c);
+    if (p->d_rope < 0 || p->d_rope > 256 || p->d_rope % 16)
+      return set_error(DSA_ERR_UNSUPPORTED, "d_rope = %d (0..256, multiple of 16)", p->d_rope);
+    if (p->kv_dtype != DSA_F32 && p->kv_dtype != DSA_BF16)
+      return set_error(DSA_ERR_UNSUPPORTED, "kv_dtype = %d (F32 or BF16)", p->kv_dtype);
+    if (p->out_dtype != DSA_F32 && p->out_dtype != DSA_BF16)
+      return set_error(DSA_ERR_UNSUPPORTED, "out_dtype = %d (F32 or BF16)", p->out_dtype);
+    if (!(p->sm_scale >= 0.f) || isinf(p->sm_scale))
+      return set_error(DSA_ERR_INVALID_ARG, "sm_scale must be finite and >= 0");
+  }
+  return DSA_OK;
+}
+
+Seqs seqs_of(const dsa_problem* p) {
+  return Seqs{p->cu_q, p->cu_k, p->num_seqs, p->total_q, p->total_k, p->max_k_len};
+}
+
+float scale_of(const dsa_problem* p) {
+  return p->sm_scale > 0.f ? p->sm_scale : 1.0f / sqrtf((float)(p->d_c + p->d_rope));
+}
+
+// Scratch regions after the status block.
+struct Carve {
+  size_t off = kStatusBytes;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  }
+};
+
+size_t scores_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->max_k_len * 4; }
+size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 4; }
+
+size_t ws_fused_indexer(const dsa_problem* p) {
+  Carve c;
+  c.take(scores_bytes(p));
+  return c.off;
+}
+
+size_t ws_fused_forward(const dsa_problem* p) {
+  Carve c;
+  c.take(scores_bytes(p));
+  c.take(idx_bytes(p));
+  return c.off;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return set_error(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned16(ws)) return set_error(DSA_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+  if (ws_bytes < need)
+    return set_error(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return DSA_OK;
+}
+
+#define DSA_TRY(expr)            \
+  do {                           \
+    int _rc = (expr);            \
+    if (_rc != DSA_OK) return _rc; \
+  } while (0)
+
+int check_indexer_inputs(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                         const float* w, const float* q_scale, const float* k_scale) {
+  DSA_TRY(check_ptr(q_idx, "q_idx", p->total_q == 0));
+  DSA_TRY(check_ptr(k_idx, "k_idx"));
+  DSA_TRY(check_ptr(w, "w", p->total_q == 0));
+  if (p->idx_dtype == DSA_FP8_E4M3) {
+    DSA_TRY(check_ptr(q_scale, "q_scale", p->total_q == 0));
+    DSA_TRY(check_ptr(k_scale, "k_scale"));
+  }
+  return DSA_OK;
+}
+
+IndexerArgs indexer_args(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                         const float* w, const float* q_scale, const float* k_scale,
+                         void* ws) {
+  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3;
+  return IndexerArgs{seqs_of(p), p->h_idx, p->d_idx, p->idx_dtype, q_idx, k_idx, w,
+                     fp8 ? q_scale : nullptr, fp8 ? k_scale : nullptr,
+                     static_cast<uint32_t*>(ws)};
+}
+
+int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx, const float* w,
+                      const float* q_scale, const float* k_scale, int32_t* idx, float* vals,
+                      void* ws, cudaStream_t s) {
+  Carve c;
+  float* scores = reinterpret_cast<float*>(static_cast<char*>(ws) + c.take(scores_bytes(p)));
+  IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
+  DSA_TRY(launch_indexer_scores_simt(ia, scores, p->max_k_len, s));
+  TopkArgs ta{seqs_of(p), p->top_k, scores, p->max_k_len, idx, vals, static_cast<uint32_t*>(ws)};
+  return launch_topk_rows(ta, s);
+}
+
+int run_sfa(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx, void* out,
+            float* lse, void* ws, cudaStream_t s) {
+  SfaArgs sa{seqs_of(p), p->h, p->d_c, p->d_rope, p->top_k, p->kv_dtype, p->out_dtype,
+             scale_of(p), q, kv, idx, out, lse, static_cast<uint32_t*>(ws)};
+  return launch_sfa_simt(sa, s);
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_status_str(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported problem";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case DSA_ERR_TIMEOUT: return "a bounded device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+int dsa_workspace_size(const dsa_problem* p, int op, size_t* bytes) {
+  if (!bytes) return set_error(DSA_ERR_INVALID_ARG, "bytes is NULL");
+  switch (op) {
+    case DSA_OP_INDEXER_SCORES: DSA_TRY(check_problem(p, true, false)); *bytes = kStatusBytes; break;
+    case DSA_OP_TOPK: DSA_TRY(check_problem(p, false, false)); *bytes = kStatusBytes; break;
+    case DSA_OP_FUSED_INDEXER:
+      DSA_TRY(check_problem(p, true, false));
+      *bytes = ws_fused_indexer(p);
+      break;
+    case DSA_OP_SPARSE_MLA_ATTN:
+      DSA_TRY(check_problem(p, false, true));
+      *bytes = kStatusBytes;
+      break;
+    case DSA_OP_FUSED_FORWARD:
+      DSA_TRY(check_problem(p, true, true));
+      *bytes = ws_fused_forward(p);
+      break;
+    default: return set_error(DSA_ERR_INVALID_ARG, "unknown op %d", op);
+  }
+  return DSA_OK;
+}
+
+int dsa_indexer_scores(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                       const float* w, const float* q_scale, const float* k_scale,
+                       float* scores, int64_t ld, void* ws, size_t ws_bytes, void* stream) {
+  DSA_TRY(check_problem(p, true, false));
+  DSA_TRY(check_indexer_inputs(p, q_idx, k_idx, w, q_scale, k_scale));
+  DSA_TRY(check_ptr(scores, "scores", p->total_q == 0));
+  if (ld < p->max_k_len) return set_error(DSA_ERR_INVALID_ARG, "ld < max_k_len");
+  DSA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
+  return launch_indexer_scores_simt(ia, scores, ld, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_topk(const dsa_problem* p, const float* scores, int64_t ld, int32_t* idx, float* vals,
+             void* ws, size_t ws_bytes, void* stream) {
+  DSA_TRY(check_problem(p, false, false));
+  DSA_TRY(check_ptr(scores, "scores", p->total_q == 0));
+  DSA_TRY(check_ptr(idx, "idx", p->total_q == 0));
+  DSA_TRY(check_ptr(vals, "vals", true));
+  if (ld < p->max_k_len) return set_error(DSA_ERR_INVALID_ARG, "ld < max_k_len");
+  DSA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  TopkArgs ta{seqs_of(p), p->top_k, scores, ld, idx, vals, static_cast<uint32_t*>(ws)};
+  return launch_topk_rows(ta, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                      const float* w, const float* q_scale, const float* k_scale,
+                      int32_t* idx, float* vals, void* ws, size_t ws_bytes, void* stream) {
+  DSA_TRY(check_problem(p, true, false));
+  DSA_TRY(check_indexer_inputs(p, q_idx, k_idx, w, q_scale, k_scale));
+  DSA_TRY(check_ptr(idx, "idx", p->total_q == 0));
+  DSA_TRY(check_ptr(vals, "vals", true));
+  DSA_TRY(check_ws(ws, ws_bytes, ws_fused_indexer(p)));
+  return run_fused_indexer(p, q_idx, k_idx, w, q_scale, k_scale, idx, vals, ws,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int dsa_sparse_mla_attn(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx,
+                        void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  DSA_TRY(check_problem(p, false, true));
+  DSA_TRY(check_ptr(q, "q", p->total_q == 0));
+  DSA_TRY(check_ptr(kv, "kv"));
+  DSA_TRY(check_ptr(idx, "idx", p->total_q == 0));
+  DSA_TRY(check_ptr(out, "out", p->total_q == 0));
+  DSA_TRY(check_ptr(lse, "lse", true));
+  DSA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  return run_sfa(p, q, kv, idx, out, lse, ws, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                      const float* w, const float* q_scale, const float* k_scale,
+                      const void* q, const void* kv, void* out, float* lse,
+                      int32_t* idx_out, float* vals_out, void* ws, size_t ws_bytes,
+                      void* stream) {
+  DSA_TRY(check_problem(p, true, true));
+  DSA_TRY(check_indexer_inputs(p, q_idx, k_idx, w, q_scale, k_scale));
+  DSA_TRY(check_ptr(q, "q", p->total_q == 0));
+  DSA_TRY(check_ptr(kv, "kv"));
+  DSA_TRY(check_ptr(out, "out", p->total_q == 0));
+  DSA_TRY(check_ptr(lse, "lse", true));
+  DSA_TRY(check_ptr(idx_out, "idx_out", true));
+  DSA_TRY(check_ptr(vals_out, "vals_out", true));
+  DSA_TRY(check_ws(ws, ws_bytes, ws_fused_forward(p)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* idx = idx_out;
+  if (!idx) {
+    Carve c;
+    c.take(scores_bytes(p));
+    idx = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + c.take(idx_bytes(p)));
+  }
+  DSA_TRY(run_fused_indexer(p, q_idx, k_idx, w, q_scale, k_scale, idx, vals_out, ws, s));
+  return run_sfa(p, q, kv, idx, out, lse, ws, s);
+}
+
+int dsa_clear_status(void* ws, void* stream) {
+  if (!ws) return set_error(DSA_ERR_WORKSPACE, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "clear_status: %s", cudaGetErrorString(e));
+  return DSA_OK;
+}
+
+int dsa_read_status(const void* ws, void* stream, uint32_t* flags) {
+  if (!ws || !flags) return set_error(DSA_ERR_INVALID_ARG, "ws/flags is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "read_status: %s", cudaGetErrorString(e));
+  if (*flags & DSA_FLAG_TIMEOUT) return set_error(DSA_ERR_TIMEOUT, "device wait timed out");
+  return DSA_OK;
+}
+
+int dsa_trace_begin(int capacity) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (capacity < 0) return set_error(DSA_ERR_INVALID_ARG, "capacity < 0");
+  for (size_t i = g_event_pool.size(); i < 2 * (size_t)capacity; ++i) {
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "trace: %s", cudaGetErrorString(e));
+    g_event_pool.push_back(ev);
+  }
+  g_trace.clear();
+  g_trace_cap = capacity;
+  g_trace_open = -1;
+  g_trace_on = true;
+  return DSA_OK;
+}
+
+int dsa_trace_end(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  return DSA_OK;
+}
+
+int dsa_trace_count(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  return (int)g_trace.size();
+}
+
+int dsa_trace_get(int i, char* name, int name_len, float* ms) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (i < 0 || i >= (int)g_trace.size()) return set_error(DSA_ERR_INVALID_ARG, "trace index");
+  const TraceRec& r = g_trace[i];
+  if (name && name_len > 0) {
+    strncpy(name, r.name.c_str(), (size_t)name_len - 1);
+    name[name_len - 1] = 0;
+  }
+  if (ms) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(ms, r.a, r.b);
+    if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "trace: %s", cudaGetErrorString(e));
+  }
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+// Internal declarations shared by the translation units of libdsa.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// ----------------------------------------------------------------------------
+// Workspace layout: [0, 256) status block; scratch regions follow, 256-aligned.
+constexpr size_t kStatusBytes = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Sequence layout as the kernels see it.
+struct Seqs {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int B;
+  int total_q;
+  int total_k;
+  int max_k_len;
+};
+
+struct RowInfo {
+  int b;      // sequence
+  int pos;    // position of the query in its sequence
+  int k0;     // first packed key row of the sequence
+  int L;      // keys in the sequence
+};
+
+// Packed query row t -> (sequence, position).  Returns false (and flags the
+// status word) when cu_q/cu_k are inconsistent with the descriptor.
+__device__ __forceinline__ bool query_row_info(const Seqs& s, int t, RowInfo& r,
+                                               uint32_t* status) {
+  int lo = 0, hi = s.B - 1;
+  while (lo < hi) {  // last b with cu_q[b] <= t
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(s.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int q0 = __ldg(s.cu_q + b), q1 = __ldg(s.cu_q + b + 1);
+  const int k0 = __ldg(s.cu_k + b), k1 = __ldg(s.cu_k + b + 1);
+  const int T = q1 - q0, L = k1 - k0;
+  const bool ok = t >= q0 && t < q1 && T <= L && k0 >= 0 && k1 <= s.total_k &&
+                  L <= s.max_k_len && q1 <= s.total_q;
+  if (!ok) {
+    atomicOr(status, DSA_FLAG_BAD_SEQS);
+    return false;
+  }
+  r.b = b;
+  r.pos = L - T + (t - q0);
+  r.k0 = k0;
+  r.L = L;
+  return true;
+}
+
+// ----------------------------------------------------------------------------
+// Element loads (widening to fp32).
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(__nv_fp8_e4m3 v) { return static_cast<float>(v); }
+
+__device__ __forceinline__ void store_f32(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_f32(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 folds to +0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+// ----------------------------------------------------------------------------
+// Host side: error reporting and launch tracing (defined in dsa_api.cu).
+int set_error(int code, const char* fmt, ...);
+void trace_pre(const char* name, cudaStream_t s);
+void trace_post(cudaStream_t s);
+int check_launch(const char* what);
+
+#define DSA_LAUNCH(name, stream, ...)   \
+  do {                                  \
+    ::dsa::trace_pre(name, stream);     \
+    __VA_ARGS__;                        \
+    ::dsa::trace_post(stream);          \
+  } while (0)
+
+// ----------------------------------------------------------------------------
+// Kernel launchers (each defined in its own .cu).
+struct IndexerArgs {
+  Seqs seqs;
+  int h_idx, d_idx, idx_dtype;
+  const void* q_idx;
+  const void* k_idx;
+  const float* w;
+  const float* q_scale;
+  const float* k_scale;
+  uint32_t* status;
+};
+
+int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
+                               cudaStream_t stream);
+
+struct TopkArgs {
+  Seqs seqs;
+  int top_k;
+  const float* scores;
+  int64_t ld;
+  int32_t* idx;
+  float* vals;
+  uint32_t* status;
+};
+int launch_topk_rows(const TopkArgs& a, cudaStream_t stream);
+
+struct SfaArgs {
+  Seqs seqs;
+  int h, d_c, d_rope, top_k, kv_dtype, out_dtype;
+  float scale;
+  const void* q;
+  const void* kv;
+  const int32_t* idx;
+  void* out;
+  float* lse;
+  uint32_t* status;
+};
+int launch_sfa_simt(const SfaArgs& a, cudaStream_t stream);
+
+}  // namespace dsa

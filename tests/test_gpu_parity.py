@@ -1,0 +1,178 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, on a GPU."""
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_lightning_gb300 as dsa
+from sparse_attention_lightning_gb300 import workloads as W
+from oracle import dsa_oracle as O
+from parity import check_attn_row, check_scores_row, check_topk_row, to_np, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_attention_lightning_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def to_dev(case):
+    return {k: v.cuda() for k, v in case.tensors().items()}
+
+
+def problem(case, d):
+    return dsa.Problem.from_config(case.cfg, d["cu_q"], d["cu_k"])
+
+
+def run_fused(case, d=None, ws=None):
+    d = d or to_dev(case)
+    P = problem(case, d)
+    out, lse, idx, vals = dsa.fused_forward(P, d["q_idx"], d["k_idx"], d["w"], d["q"], d["kv"],
+                                            d.get("q_scale"), d.get("k_scale"), want_vals=True,
+                                            ws=ws)
+    torch.cuda.synchronize()
+    return P, out, lse, idx, vals
+
+
+def check_rows(case, idx, vals, out, lse, rows):
+    """Top-K, selected scores and attention of `rows` against the oracle."""
+    p = O.problem_from_case(case)
+    tol = tol_for(case.cfg)
+    idx_n, vals_n, out_n, lse_n = to_np(idx), to_np(vals), to_np(out), to_np(lse)
+    swaps = 0
+    for t in rows:
+        I = p.scores(t)
+        ctx = f"{case.cfg.name} row {t}"
+        swaps += check_topk_row(idx_n[t], I, case.cfg.top_k, ctx)["swaps"]
+        n = min(case.cfg.top_k, I.shape[0])
+        sel = idx_n[t, :n]
+        m = np.abs(I).max()
+        assert np.abs(vals_n[t, :n] - I[sel]).max() <= 1e-2 * m + 1e-30, ctx + ": vals"
+        assert np.all(np.isneginf(vals_n[t, n:]))
+        ref_out, ref_lse = p.sfa(t, sel)
+        check_attn_row(out_n[t], lse_n[t], ref_out, ref_lse, tol, ctx)
+    return swaps
+
+
+def test_tiny_prefill_fp32_all_rows():
+    case = W.make_case(W.tiny_prefill(), W.WORKLOAD_SEEDS["tiny_prefill"])
+    P, out, lse, idx, vals = run_fused(case)
+    check_rows(case, idx, vals, out, lse, range(case.cfg.total_q))
+
+
+SMALL = [
+    # (q_lens, k_lens, dims, dtypes) — ragged tails, L < k, L = 1, T = L and T < L
+    ([1, 7, 40, 1], [1, 300, 40, 2049], dict(top_k=32), ("f32", "f32")),
+    ([3, 1, 130], [3, 77, 130], dict(top_k=64), ("bf16", "bf16")),
+    ([1, 2, 1], [5000, 133, 2100], dict(h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64,
+                                        top_k=2048), ("bf16", "bf16")),
+    ([1, 1, 4], [4100, 3000, 300], dict(h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64,
+                                        top_k=2048), ("e4m3", "bf16")),
+    ([2, 1], [9, 65], dict(h_idx=3, d_idx=48, h=5, d_c=32, d_rope=16, top_k=5), ("e4m3", "f32")),
+]
+
+
+@pytest.mark.parametrize("qs,ks,dims,dts", SMALL)
+def test_small_cases(qs, ks, dims, dts):
+    cfg = W.custom(qs, ks, idx_dtype=dts[0], kv_dtype=dts[1], **dims)
+    case = W.make_case(cfg, seed=123)
+    P, out, lse, idx, vals = run_fused(case)
+    check_rows(case, idx, vals, out, lse, range(cfg.total_q))
+
+
+def test_materialised_scores_and_standalone_topk():
+    cfg = W.custom([1, 5, 33], [700, 5, 100], h_idx=8, d_idx=64, idx_dtype="bf16",
+                   kv_dtype="bf16", top_k=16)
+    case = W.make_case(cfg, seed=7)
+    d = to_dev(case)
+    P = problem(case, d)
+    s = dsa.indexer_scores(P, d["q_idx"], d["k_idx"], d["w"])
+    idx, vals = dsa.topk(P, s, want_vals=True)
+    torch.cuda.synchronize()
+    p = O.problem_from_case(case)
+    sn, idn = to_np(s), to_np(idx)
+    for t in range(cfg.total_q):
+        I = p.scores(t)
+        check_scores_row(sn[t], I, f"row {t}")
+        check_topk_row(idn[t], I, cfg.top_k, f"row {t}")
+
+
+def test_topk_ties_match_oracle_exactly():
+    # integer-valued scores with many ties: the tie rule (smaller position) fixes the set
+    cfg = W.custom([3], [3000], top_k=100)
+    case = W.make_case(cfg, seed=1)
+    d = to_dev(case)
+    P = problem(case, d)
+    g = torch.Generator().manual_seed(3)
+    scores = torch.randint(0, 6, (3, 3000), generator=g).to(torch.float32)
+    idx, vals = dsa.topk(P, scores.cuda(), want_vals=True)
+    torch.cuda.synchronize()
+    for t in range(3):
+        pos = 3000 - 3 + t
+        ref = np.sort(O.topk_row(scores[t, :pos + 1].double().numpy(), 100))
+        assert np.array_equal(to_np(idx)[t], ref)
+
+
+def test_sfa_flags_bad_indices_and_skips_them():
+    cfg = W.custom([2], [50], top_k=8, kv_dtype="bf16")
+    case = W.make_case(cfg, seed=5)
+    d = to_dev(case)
+    P = problem(case, d)
+    idx = torch.tensor([[3, -1, 49, 7, 60, 2, -1, 0],        # 49 > pos 48, 60 out of range
+                        [-1, -1, -1, -1, -1, -1, -1, -1]], dtype=torch.int32).cuda()
+    ws = dsa.Workspace()
+    ws.clear_status()
+    out, lse = dsa.sparse_mla_attn(P, d["q"], d["kv"], idx, ws=ws)
+    flags = ws.status()
+    assert flags & 0x1, "DSA_FLAG_BAD_INDEX not set"
+    p = O.problem_from_case(case)
+    ref_out, ref_lse = p.sfa(0, [3, 7, 2, 0])
+    check_attn_row(to_np(out)[0], to_np(lse)[0], ref_out, ref_lse, tol_for(cfg))
+    assert np.all(to_np(out)[1] == 0) and np.all(np.isneginf(to_np(lse)[1]))
+    ws.clear_status()
+    assert ws.status() == 0
+
+
+def test_repeat_runs_are_bitwise_identical():
+    cfg = W.custom([1, 1], [3000, 2500], h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64,
+                   top_k=2048, idx_dtype="bf16", kv_dtype="bf16")
+    case = W.make_case(cfg, seed=9)
+    d = to_dev(case)
+    r1 = run_fused(case, d)
+    r2 = run_fused(case, d)
+    assert torch.equal(r1[3], r2[3])
+    assert torch.equal(r1[1].view(torch.int16), r2[1].view(torch.int16))
+
+
+def test_decode_workload_full_size():
+    """The bench's decode workload (B=32, L ~ U[8192, 32768], bf16), every row checked."""
+    cfg = W.workload("decode")
+    case = W.make_case(cfg, W.WORKLOAD_SEEDS["decode"])
+    P, out, lse, idx, vals = run_fused(case)
+    check_rows(case, idx, vals, out, lse, range(cfg.total_q))
+
+
+def _sample_rows(T, k, n_random=24, seed=0):
+    fixed = {0, 1, k - 2, k - 1, k, T // 2, T - 2, T - 1}
+    rng = np.random.default_rng(seed)
+    return sorted(fixed | set(rng.integers(0, T, n_random).tolist()))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefill_8k", "prefill_64k"])
+def test_prefill_workloads_sampled_rows(name):
+    cfg = W.workload(name)
+    case = W.make_case(cfg, W.WORKLOAD_SEEDS[name])
+    P, out, lse, idx, vals = run_fused(case)
+    check_rows(case, idx, vals, out, lse, _sample_rows(cfg.total_q, cfg.top_k))
+
+
+@pytest.mark.slow
+def test_fp8_decode_workload_sampled_sequences():
+    cfg = W.workload("fp8_decode")
+    case = W.make_case(cfg, W.WORKLOAD_SEEDS["fp8_decode"])
+    P, out, lse, idx, vals = run_fused(case)
+    rows = sorted(set(np.random.default_rng(4).integers(0, cfg.total_q, 14).tolist()) | {0, 127})
+    check_rows(case, idx, vals, out, lse, rows)
