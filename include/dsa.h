@@ -186,6 +186,30 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
                       int32_t* idx_out, float* vals_out, void* ws, size_t ws_bytes,
                       void* stream);
 
+/*
+ * dsa_fused_indexer_static: dsa_fused_indexer for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this call; it exists for
+ * code that runs inside a host framework owning all device memory (a fixed
+ * budget or its own caching allocator, raw cudaMalloc forbidden) and for
+ * latency-critical loops where cudaMalloc/cudaFree would synchronise the
+ * device.  Such callers pass inputs and outputs but no workspace.
+ *
+ * Scratch is a static device array inside the library: a 256-byte status block
+ * plus room for 4,194,304 fp32 scores (16 MiB), held by every device that loads
+ * the library until the process exits.  Problems with total_q * max_k_len above
+ * 4,194,304 are rejected with DSA_ERR_UNSUPPORTED.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).  Its first call on a
+ * device looks up the array's address with that device current; make that first
+ * call before any stream capture.  All calls on one device share the array:
+ * calls that overlap on the GPU race, and the array keeps the last call's
+ * contents.  Each call zeroes the status block first; if flags_out (device
+ * memory, may be NULL) is given, the call's DSA_FLAG_* bits are copied there
+ * at its end.  Other arguments and results are those of dsa_fused_indexer.
+ */
+int dsa_fused_indexer_static(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                             const float* w, const float* q_scale, const float* k_scale,
+                             int32_t* idx, float* vals, uint32_t* flags_out, void* stream);
+
 /* Zero the workspace status word (enqueued on `stream`). */
 int dsa_clear_status(void* ws, void* stream);
 
