@@ -34,6 +34,49 @@ int check_launch(const char* what) {
 }
 
 // ----------------------------------------------------------------------------
+// Device properties and tensor maps.
+int num_sms() {
+  static int n[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 1;
+  }
+  return n[dev];
+}
+
+int make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                 uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+      return set_error(DSA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    fn = reinterpret_cast<EncodeFn>(f);
+  }
+  if (rows == 0) rows = 1;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DSA_OK;
+}
+
+// ----------------------------------------------------------------------------
 // Launch tracing: an event pair around each launch while enabled.
 namespace {
 struct TraceRec {
@@ -141,16 +184,33 @@ struct Carve {
 size_t scores_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->max_k_len * 4; }
 size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 4; }
 
-size_t ws_fused_indexer(const dsa_problem* p) {
+// Fused indexer scratch: scores [total_q, max_k_len] f32, then the per-row tile
+// starts of the tensor-core schedule.  The fused forward adds the indices.
+struct IndexerScratch {
+  float* scores;
+  int32_t* tile_start;
+  int32_t* idx;
+};
+
+size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
-  c.take(scores_bytes(p));
+  const size_t o_scores = c.take(scores_bytes(p));
+  const size_t o_tiles = c.take(indexer_tc_tile_start_bytes(p->total_q));
+  const size_t o_idx = c.take(idx_bytes(p));
+  if (out) {
+    char* b = static_cast<char*>(ws);
+    out->scores = reinterpret_cast<float*>(b + o_scores);
+    out->tile_start = reinterpret_cast<int32_t*>(b + o_tiles);
+    out->idx = reinterpret_cast<int32_t*>(b + o_idx);
+  }
   return c.off;
 }
 
-size_t ws_fused_forward(const dsa_problem* p) {
+size_t ws_fused_indexer(const dsa_problem* p) { return carve_indexer(p, nullptr, nullptr); }
+size_t ws_fused_forward(const dsa_problem* p) { return carve_indexer(p, nullptr, nullptr); }
+size_t ws_indexer_scores(const dsa_problem* p) {
   Carve c;
-  c.take(scores_bytes(p));
-  c.take(idx_bytes(p));
+  c.take(indexer_tc_tile_start_bytes(p->total_q));
   return c.off;
 }
 
@@ -189,15 +249,24 @@ IndexerArgs indexer_args(const dsa_problem* p, const void* q_idx, const void* k_
                      static_cast<uint32_t*>(ws)};
 }
 
+int run_topk(const TopkArgs& ta, cudaStream_t s) {
+  if (ta.seqs.max_k_len <= topk_smem_max_keys()) return launch_topk_smem(ta, s);
+  return launch_topk_rows(ta, s);
+}
+
 int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx, const float* w,
                       const float* q_scale, const float* k_scale, int32_t* idx, float* vals,
                       void* ws, cudaStream_t s) {
-  Carve c;
-  float* scores = reinterpret_cast<float*>(static_cast<char*>(ws) + c.take(scores_bytes(p)));
+  IndexerScratch sc;
+  carve_indexer(p, ws, &sc);
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
-  DSA_TRY(launch_indexer_scores_simt(ia, scores, p->max_k_len, s));
-  TopkArgs ta{seqs_of(p), p->top_k, scores, p->max_k_len, idx, vals, static_cast<uint32_t*>(ws)};
-  return launch_topk_rows(ta, s);
+  if (indexer_tc_eligible(ia))
+    DSA_TRY(launch_indexer_tc(ia, sc.scores, p->max_k_len, sc.tile_start, s));
+  else
+    DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, p->max_k_len, s));
+  TopkArgs ta{seqs_of(p), p->top_k, sc.scores, p->max_k_len, idx, vals,
+              static_cast<uint32_t*>(ws)};
+  return run_topk(ta, s);
 }
 
 int run_sfa(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx, void* out,
@@ -233,7 +302,10 @@ const char* dsa_last_error(void) { return g_last_error.c_str(); }
 int dsa_workspace_size(const dsa_problem* p, int op, size_t* bytes) {
   if (!bytes) return set_error(DSA_ERR_INVALID_ARG, "bytes is NULL");
   switch (op) {
-    case DSA_OP_INDEXER_SCORES: DSA_TRY(check_problem(p, true, false)); *bytes = kStatusBytes; break;
+    case DSA_OP_INDEXER_SCORES:
+      DSA_TRY(check_problem(p, true, false));
+      *bytes = ws_indexer_scores(p);
+      break;
     case DSA_OP_TOPK: DSA_TRY(check_problem(p, false, false)); *bytes = kStatusBytes; break;
     case DSA_OP_FUSED_INDEXER:
       DSA_TRY(check_problem(p, true, false));
@@ -259,9 +331,17 @@ int dsa_indexer_scores(const dsa_problem* p, const void* q_idx, const void* k_id
   DSA_TRY(check_indexer_inputs(p, q_idx, k_idx, w, q_scale, k_scale));
   DSA_TRY(check_ptr(scores, "scores", p->total_q == 0));
   if (ld < p->max_k_len) return set_error(DSA_ERR_INVALID_ARG, "ld < max_k_len");
-  DSA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
+  DSA_TRY(check_ws(ws, ws_bytes, ws_indexer_scores(p)));
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
-  return launch_indexer_scores_simt(ia, scores, ld, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (indexer_tc_eligible(ia)) {
+    Carve c;
+    int32_t* tiles = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
+                                                c.take(indexer_tc_tile_start_bytes(p->total_q)));
+    DSA_TRY(launch_indexer_tc(ia, scores, ld, tiles, s));
+    return launch_mask_tail(seqs_of(p), scores, ld, static_cast<uint32_t*>(ws), s);
+  }
+  return launch_indexer_scores_simt(ia, scores, ld, s);
 }
 
 int dsa_topk(const dsa_problem* p, const float* scores, int64_t ld, int32_t* idx, float* vals,
@@ -273,7 +353,7 @@ int dsa_topk(const dsa_problem* p, const float* scores, int64_t ld, int32_t* idx
   if (ld < p->max_k_len) return set_error(DSA_ERR_INVALID_ARG, "ld < max_k_len");
   DSA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
   TopkArgs ta{seqs_of(p), p->top_k, scores, ld, idx, vals, static_cast<uint32_t*>(ws)};
-  return launch_topk_rows(ta, static_cast<cudaStream_t>(stream));
+  return run_topk(ta, static_cast<cudaStream_t>(stream));
 }
 
 int dsa_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx,
@@ -317,9 +397,9 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* idx = idx_out;
   if (!idx) {
-    Carve c;
-    c.take(scores_bytes(p));
-    idx = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + c.take(idx_bytes(p)));
+    IndexerScratch sc;
+    carve_indexer(p, ws, &sc);
+    idx = sc.idx;
   }
   DSA_TRY(run_fused_indexer(p, q_idx, k_idx, w, q_scale, k_scale, idx, vals_out, ws, s));
   return run_sfa(p, q, kv, idx, out, lse, ws, s);

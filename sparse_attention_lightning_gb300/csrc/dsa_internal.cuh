@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libdsa.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -85,6 +86,12 @@ void trace_pre(const char* name, cudaStream_t s);
 void trace_post(cudaStream_t s);
 int check_launch(const char* what);
 
+// A 2-D tiled tensor map (128-byte swizzle, 256-byte L2 promotion, zero fill):
+// `rows` rows of `inner` elements, `row_bytes` apart; box = box_inner x box_rows.
+int make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                 uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+int num_sms();
+
 #define DSA_LAUNCH(name, stream, ...)   \
   do {                                  \
     ::dsa::trace_pre(name, stream);     \
@@ -108,6 +115,16 @@ struct IndexerArgs {
 int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
                                cudaStream_t stream);
 
+// tcgen05 indexer (H_I = 64, d_I = 128, bf16 or FP8): writes scores[t, s] for s <= pos(t).
+bool indexer_tc_eligible(const IndexerArgs& a);
+size_t indexer_tc_tile_start_bytes(int total_q);
+int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, int32_t* tile_start,
+                      cudaStream_t stream);
+
+// Fill scores[t, s] = -inf for pos(t) < s < ld.
+int launch_mask_tail(const Seqs& seqs, float* scores, int64_t ld, uint32_t* status,
+                     cudaStream_t stream);
+
 struct TopkArgs {
   Seqs seqs;
   int top_k;
@@ -118,6 +135,9 @@ struct TopkArgs {
   uint32_t* status;
 };
 int launch_topk_rows(const TopkArgs& a, cudaStream_t stream);
+// Shared-memory-resident variant for rows of at most topk_smem_max_keys() keys.
+int topk_smem_max_keys();
+int launch_topk_smem(const TopkArgs& a, cudaStream_t stream);
 
 struct SfaArgs {
   Seqs seqs;

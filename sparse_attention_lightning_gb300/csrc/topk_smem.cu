@@ -1,0 +1,251 @@
+// Causal Top-K of a score row held entirely in shared memory (rows up to
+// 40,960 keys): one CTA per query row.
+//
+// Top-K selection of the Lightning Indexer ("Day0 Inference Adaptation and
+// Performance Optimization for New-Architecture LLMs", §4.1), with the same
+// contract as topk_rows.cu: the n = min(top_k, pos+1) largest scores, ties to
+// the smaller position, written in ascending position order, -1 padded.
+//
+// The row is read once from global memory into shared memory as
+// order-preserving uint32 keys, with its min and max.  Radix digits start just
+// below the bits all keys share (so the first 8-bit digit already spreads the
+// row over up to 256 bins), with per-warp histograms to keep shared-memory
+// atomics uncontended.  Once the keys still in play fit a small buffer they
+// are compacted and later digits scan only them.  A single block-wide prefix
+// sum then places every selected position: each thread owns a contiguous run
+// of keys, read in a lane-rotated order so the 32 lanes never share a bank.
+#include "dsa_internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kT = 512;
+constexpr int kW = kT / 32;
+constexpr int kMaxKeys = 40960;
+constexpr int kCandCap = 4096;
+constexpr size_t kSmem = sizeof(uint32_t) * ((size_t)kMaxKeys + kW * 256 + 256 + kCandCap);
+
+__device__ __forceinline__ uint32_t scan_excl(uint32_t v, uint32_t* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t s = lane < kW ? warp_sums[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < kW) warp_sums[lane] = s;
+  }
+  __syncthreads();
+  return (warp ? warp_sums[warp - 1] : 0u) + x - v;
+}
+
+__global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* keys = sm;                  // [kMaxKeys]
+  uint32_t* hist = keys + kMaxKeys;     // [kW][256]
+  uint32_t* tot = hist + kW * 256;      // [256]
+  uint32_t* cand = tot + 256;           // [kCandCap]
+  __shared__ uint32_t red_min[kW], red_max[kW], warp_sums[kW];
+  __shared__ uint32_t s_digit, s_above, s_cnt, s_ncand;
+
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  RowInfo r;
+  if (!query_row_info(a.seqs, t, r, a.status)) return;
+  const float* row = a.scores + (int64_t)t * a.ld;
+  const int n = r.pos + 1;
+  const int k = min(a.top_k, n);
+  int32_t* idx = a.idx + (int64_t)t * a.top_k;
+  float* vals = a.vals ? a.vals + (int64_t)t * a.top_k : nullptr;
+  for (int j = k + tid; j < a.top_k; j += kT) {
+    idx[j] = -1;
+    if (vals) vals[j] = -INFINITY;
+  }
+  if (k == n) {
+    for (int i = tid; i < n; i += kT) {
+      idx[i] = i;
+      if (vals) vals[i] = row[i];
+    }
+    return;
+  }
+
+  // --- load the row as keys, with its min and max ----------------------------
+  uint32_t lmin = 0xffffffffu, lmax = 0u;
+  for (int i = tid; i < n; i += kT) {
+    const uint32_t key = order_key(row[i]);
+    keys[i] = key;
+    lmin = min(lmin, key);
+    lmax = max(lmax, key);
+  }
+  lmin = __reduce_min_sync(0xffffffffu, lmin);
+  lmax = __reduce_max_sync(0xffffffffu, lmax);
+  if (lane == 0) { red_min[warp] = lmin; red_max[warp] = lmax; }
+  __syncthreads();
+  uint32_t kmin = red_min[0], kmax = red_max[0];
+  for (int w = 1; w < kW; ++w) { kmin = min(kmin, red_min[w]); kmax = max(kmax, red_max[w]); }
+
+  // --- radix select of the exact n-th largest key -------------------------------
+  uint32_t prefix = kmax, need = (uint32_t)k;
+  if (kmin != kmax) {
+    int hb = 31 - __clz(kmax ^ kmin);                     // highest bit that differs
+    uint32_t mask = hb == 31 ? 0u : ~((2u << hb) - 1u);   // bits shared by every key
+    prefix = kmax & mask;
+    const uint32_t* src = keys;
+    int src_n = n;
+    bool compacted = false;
+    while (true) {
+      const int shift = hb >= 7 ? hb - 7 : 0;
+      const int nb = hb - shift + 1;
+      const uint32_t dmask = (nb == 32) ? 0xffffffffu : ((1u << nb) - 1u);
+      for (int i = tid; i < kW * 256; i += kT) hist[i] = 0;
+      __syncthreads();
+      uint32_t* h = hist + warp * 256;
+      for (int i = tid; i < src_n; i += kT) {
+        const uint32_t key = src[i];
+        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & dmask], 1u);
+      }
+      __syncthreads();
+      if (tid < 256) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) c += hist[w * 256 + tid];
+        tot[tid] = c;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { c[i] = tot[255 - 8 * lane - i]; sum += c[i]; }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= need && excl < need);
+        if (hit && lane == __ffs(hit) - 1) {
+          uint32_t run = excl;
+          for (int i = 0; i < 8; ++i) {
+            if (run + c[i] >= need) {
+              s_digit = 255 - 8 * lane - i;
+              s_above = run;
+              s_cnt = c[i];
+              break;
+            }
+            run += c[i];
+          }
+        }
+      }
+      __syncthreads();
+      need -= s_above;
+      prefix |= s_digit << shift;
+      mask |= dmask << shift;
+      const uint32_t cnt = s_cnt;
+      if (shift == 0) break;
+      hb = shift - 1;
+      if (!compacted && cnt <= (uint32_t)kCandCap) {
+        if (tid == 0) s_ncand = 0;
+        __syncthreads();
+        for (int i = tid; i < n; i += kT) {
+          const uint32_t key = keys[i];
+          if ((key & mask) == prefix) cand[atomicAdd(&s_ncand, 1u)] = key;
+        }
+        __syncthreads();
+        src = cand;
+        src_n = (int)s_ncand;
+        compacted = true;
+      }
+    }
+  }
+  const uint32_t T = prefix;  // the n-th largest key; `need` of the keys equal to it are kept
+
+  // --- ordered write -------------------------------------------------------------------
+  const int m = (n + 32 * kT - 1) / (32 * kT);  // 32-key chunks per thread
+  const int base = tid * 32 * m;
+  uint32_t cg = 0, ce = 0;
+  for (int c = 0; c < m; ++c) {
+#pragma unroll 8
+    for (int jj = 0; jj < 32; ++jj) {
+      const int i = base + c * 32 + ((jj + lane) & 31);
+      if (i < n) {
+        const uint32_t key = keys[i];
+        cg += key > T;
+        ce += key == T;
+      }
+    }
+  }
+  const uint32_t pre = scan_excl(cg | (ce << 16), warp_sums);
+  uint32_t g_off = pre & 0xffffu, e_off = pre >> 16;
+  for (int c = 0; c < m; ++c) {
+    uint32_t gtm = 0, eqm = 0;
+#pragma unroll 8
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = (jj + lane) & 31;
+      const int i = base + c * 32 + j;
+      if (i < n) {
+        const uint32_t key = keys[i];
+        if (key > T) gtm |= 1u << j;
+        else if (key == T) eqm |= 1u << j;
+      }
+    }
+    const uint32_t sel = gtm | eqm;
+    if (sel) {
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = (jj + lane) & 31;
+        const uint32_t bit = 1u << j, low = bit - 1u;
+        if (!(sel & bit)) continue;
+        const uint32_t gb = g_off + __popc(gtm & low), eb = e_off + __popc(eqm & low);
+        int slot = -1;
+        if (gtm & bit) slot = (int)(gb + min(eb, need));
+        else if (eb < need) slot = (int)(gb + eb);
+        if (slot >= 0) {
+          const int i = base + c * 32 + j;
+          idx[slot] = i;
+          if (vals) vals[slot] = key_to_float(keys[i]);
+        }
+      }
+    }
+    g_off += __popc(gtm);
+    e_off += __popc(eqm);
+  }
+}
+
+__global__ void mask_tail_kernel(Seqs seqs, float* scores, int64_t ld, uint32_t* status) {
+  RowInfo r;
+  const int t = blockIdx.x;
+  if (!query_row_info(seqs, t, r, status)) return;
+  float* row = scores + (int64_t)t * ld;
+  for (int64_t s = r.pos + 1 + threadIdx.x; s < ld; s += blockDim.x) row[s] = -INFINITY;
+}
+
+}  // namespace
+
+int topk_smem_max_keys() { return kMaxKeys; }
+
+int launch_topk_smem(const TopkArgs& a, cudaStream_t stream) {
+  if (a.seqs.total_q == 0) return DSA_OK;
+  if (cudaFuncSetAttribute(topk_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmem) != cudaSuccess)
+    return check_launch("topk_smem: smem attribute");
+  DSA_LAUNCH("topk_smem", stream, topk_smem_kernel<<<a.seqs.total_q, kT, kSmem, stream>>>(a));
+  return check_launch("topk_smem");
+}
+
+int launch_mask_tail(const Seqs& seqs, float* scores, int64_t ld, uint32_t* status,
+                     cudaStream_t stream) {
+  if (seqs.total_q == 0) return DSA_OK;
+  DSA_LAUNCH("mask_tail", stream,
+             mask_tail_kernel<<<seqs.total_q, 256, 0, stream>>>(seqs, scores, ld, status));
+  return check_launch("mask_tail");
+}
+
+}  // namespace dsa

@@ -99,6 +99,28 @@ def test_materialised_scores_and_standalone_topk():
         check_topk_row(idn[t], I, cfg.top_k, f"row {t}")
 
 
+@pytest.mark.parametrize("idx_dtype", ["bf16", "e4m3"])
+def test_tensor_core_indexer_scores(idx_dtype):
+    # H_I = 64, d_I = 128 runs on tcgen05; rows cover decode (T=1), T<L and prefill,
+    # tails that are not multiples of the 128-key tile, and a 1-key history.
+    cfg = W.custom([1, 3, 130, 1], [1000, 300, 130, 1], h_idx=64, d_idx=128, h=8, d_c=64,
+                   d_rope=16, top_k=64, idx_dtype=idx_dtype, kv_dtype="bf16")
+    case = W.make_case(cfg, seed=17)
+    d = to_dev(case)
+    P = problem(case, d)
+    s = dsa.indexer_scores(P, d["q_idx"], d["k_idx"], d["w"], d.get("q_scale"), d.get("k_scale"))
+    idx, _ = dsa.topk(P, s)
+    torch.cuda.synchronize()
+    p = O.problem_from_case(case)
+    sn, idn = to_np(s), to_np(idx)
+    worst = 0.0
+    for t in range(cfg.total_q):
+        I = p.scores(t)
+        worst = max(worst, check_scores_row(sn[t], I, f"row {t}"))
+        check_topk_row(idn[t], I, cfg.top_k, f"row {t}")
+    assert worst < 1e-4, worst  # fp32 accumulation of exact products: far inside 1e-2
+
+
 def test_topk_ties_match_oracle_exactly():
     # integer-valued scores with many ties: the tie rule (smaller position) fixes the set
     cfg = W.custom([3], [3000], top_k=100)
