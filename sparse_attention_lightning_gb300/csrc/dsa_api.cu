@@ -181,7 +181,9 @@ struct Carve {
   }
 };
 
-size_t scores_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->max_k_len * 4; }
+// Workspace score rows are padded to 32 floats (128 B) so every row is aligned.
+int64_t scores_ld(const dsa_problem* p) { return ((int64_t)p->max_k_len + 31) / 32 * 32; }
+size_t scores_bytes(const dsa_problem* p) { return (size_t)p->total_q * scores_ld(p) * 4; }
 size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 4; }
 
 // Fused indexer scratch: scores [total_q, max_k_len] f32, then the per-row tile
@@ -190,24 +192,38 @@ struct IndexerScratch {
   float* scores;
   int32_t* tile_start;
   int32_t* idx;
+  void* sfa;
 };
+
+// SFA scratch (split-row partials of the tensor-core path; 0 bytes otherwise).
+size_t sfa_scratch_bytes(const dsa_problem* p) {
+  const bool tc = p->kv_dtype == DSA_BF16 && p->h == 128 && p->d_c == 512 && p->d_rope == 64;
+  return tc ? sfa_tc_scratch_bytes(p->total_q) : 0;
+}
 
 size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
   const size_t o_scores = c.take(scores_bytes(p));
   const size_t o_tiles = c.take(indexer_tc_tile_start_bytes(p->total_q));
   const size_t o_idx = c.take(idx_bytes(p));
+  const size_t o_sfa = c.take(sfa_scratch_bytes(p));
   if (out) {
     char* b = static_cast<char*>(ws);
     out->scores = reinterpret_cast<float*>(b + o_scores);
     out->tile_start = reinterpret_cast<int32_t*>(b + o_tiles);
     out->idx = reinterpret_cast<int32_t*>(b + o_idx);
+    out->sfa = b + o_sfa;
   }
   return c.off;
 }
 
 size_t ws_fused_indexer(const dsa_problem* p) { return carve_indexer(p, nullptr, nullptr); }
 size_t ws_fused_forward(const dsa_problem* p) { return carve_indexer(p, nullptr, nullptr); }
+size_t ws_sfa(const dsa_problem* p) {
+  Carve c;
+  c.take(sfa_scratch_bytes(p));
+  return c.off;
+}
 size_t ws_indexer_scores(const dsa_problem* p) {
   Carve c;
   c.take(indexer_tc_tile_start_bytes(p->total_q));
@@ -260,19 +276,20 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
   IndexerScratch sc;
   carve_indexer(p, ws, &sc);
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
+  const int64_t ld = scores_ld(p);
   if (indexer_tc_eligible(ia))
-    DSA_TRY(launch_indexer_tc(ia, sc.scores, p->max_k_len, sc.tile_start, s));
+    DSA_TRY(launch_indexer_tc(ia, sc.scores, ld, sc.tile_start, s));
   else
-    DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, p->max_k_len, s));
-  TopkArgs ta{seqs_of(p), p->top_k, sc.scores, p->max_k_len, idx, vals,
-              static_cast<uint32_t*>(ws)};
+    DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, ld, s));
+  TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws)};
   return run_topk(ta, s);
 }
 
 int run_sfa(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx, void* out,
-            float* lse, void* ws, cudaStream_t s) {
+            float* lse, void* ws, void* scratch, cudaStream_t s) {
   SfaArgs sa{seqs_of(p), p->h, p->d_c, p->d_rope, p->top_k, p->kv_dtype, p->out_dtype,
              scale_of(p), q, kv, idx, out, lse, static_cast<uint32_t*>(ws)};
+  if (sfa_tc_eligible(sa)) return launch_sfa_tc(sa, scratch, s);
   return launch_sfa_simt(sa, s);
 }
 
@@ -313,7 +330,7 @@ int dsa_workspace_size(const dsa_problem* p, int op, size_t* bytes) {
       break;
     case DSA_OP_SPARSE_MLA_ATTN:
       DSA_TRY(check_problem(p, false, true));
-      *bytes = kStatusBytes;
+      *bytes = ws_sfa(p);
       break;
     case DSA_OP_FUSED_FORWARD:
       DSA_TRY(check_problem(p, true, true));
@@ -376,8 +393,10 @@ int dsa_sparse_mla_attn(const dsa_problem* p, const void* q, const void* kv, con
   DSA_TRY(check_ptr(idx, "idx", p->total_q == 0));
   DSA_TRY(check_ptr(out, "out", p->total_q == 0));
   DSA_TRY(check_ptr(lse, "lse", true));
-  DSA_TRY(check_ws(ws, ws_bytes, kStatusBytes));
-  return run_sfa(p, q, kv, idx, out, lse, ws, static_cast<cudaStream_t>(stream));
+  DSA_TRY(check_ws(ws, ws_bytes, ws_sfa(p)));
+  Carve c;
+  void* scratch = static_cast<char*>(ws) + c.take(sfa_scratch_bytes(p));
+  return run_sfa(p, q, kv, idx, out, lse, ws, scratch, static_cast<cudaStream_t>(stream));
 }
 
 int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx,
@@ -395,14 +414,11 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
   DSA_TRY(check_ptr(vals_out, "vals_out", true));
   DSA_TRY(check_ws(ws, ws_bytes, ws_fused_forward(p)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t* idx = idx_out;
-  if (!idx) {
-    IndexerScratch sc;
-    carve_indexer(p, ws, &sc);
-    idx = sc.idx;
-  }
+  IndexerScratch sc;
+  carve_indexer(p, ws, &sc);
+  int32_t* idx = idx_out ? idx_out : sc.idx;
   DSA_TRY(run_fused_indexer(p, q_idx, k_idx, w, q_scale, k_scale, idx, vals_out, ws, s));
-  return run_sfa(p, q, kv, idx, out, lse, ws, s);
+  return run_sfa(p, q, kv, idx, out, lse, ws, sc.sfa, s);
 }
 
 int dsa_clear_status(void* ws, void* stream) {

@@ -152,4 +152,9 @@ struct SfaArgs {
 };
 int launch_sfa_simt(const SfaArgs& a, cudaStream_t stream);
 
+// tcgen05 SFA (H = 128, d_c = 512, d_rope = 64, bf16) on 2-CTA clusters.
+bool sfa_tc_eligible(const SfaArgs& a);
+size_t sfa_tc_scratch_bytes(int total_q);
+int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream);
+
 }  // namespace dsa

@@ -1,0 +1,566 @@
+// Sparse Flash Attention over the MLA latent cache on tcgen05 tensor cores,
+// for H = 128 query heads, latent d_c = 512 + rope 64 (D = 576), bf16.
+//
+// ("Day0 Inference Adaptation and Performance Optimization for New-Architecture
+// LLMs", §2.2 and §4.1: the sparse attention core gathers the latent rows at the
+// Top-K positions and attends over them chunk by chunk, IO-aware; "Day0 Inference
+// Adaptation and Performance Optimization for a New Architecture Domestic LLM on
+// Ascend", §4: SFA reads the KV cache at the indexer's position set.)
+//
+//   S[h, i] = scale · q[t,h,:] · kv[row_i, :]        (all 576 columns)
+//   out[t,h,:] = Σ_i softmax_i(S[h,:]) · kv[row_i, 0:512],  lse[t,h] = log Σ_i exp S[h,i]
+//
+// Why a CTA pair.  All 128 heads share each gathered latent row, so heads are
+// the MMA's M = 128.  A single CTA would need the whole query block (128 x 576
+// bf16 = 144 KB of shared memory) and a 128 x 512 fp32 output accumulator, which
+// is all 512 TMEM columns with no room for the logits.  So a 2-CTA cluster splits
+// the columns: CTA 0 owns latent columns 0..255, CTA 1 owns latent 256..511 plus
+// the 64 rope columns.  Each CTA gathers only its columns of every selected row,
+// computes a partial S over them, and the two partial S tiles are added through
+// distributed shared memory (same order in both CTAs, so both hold identical
+// logits and take identical softmax decisions).  Each CTA then multiplies P by its
+// own 256 value columns: O_half (128 x 256 fp32) lives in TMEM next to a
+// double-buffered 128 x 64 S tile.
+//
+// Per chunk of 64 selected rows: TMA tile::gather4 loads (4 rows x 128 B per
+// instruction, 128-byte swizzle) into a 2-stage ring; S = Q_half · KV_half^T
+// (M=128, N=64, K=256|320, K-major operands); the softmax warps (one thread per
+// head) read S from TMEM, exchange halves with the peer CTA, keep a running max
+// (the output is rescaled only when the max grows by more than 2^8), write
+// P = exp2(x - m) as bf16 into shared memory; O += P · V (M=128, N=256, K=64,
+// V read MN-major straight from the gathered tile).
+//
+// Decode rows are split over 2-4 clusters when there are few queries; the last
+// cluster of a row to finish merges the partial (O, max, sum) of the others.
+// Every wait is bounded (DSA_FLAG_TIMEOUT).
+#include "dsa_internal.cuh"
+#include "tc_sm100.cuh"
+
+namespace dsa {
+namespace {
+
+using namespace tc;
+
+constexpr int kH = 128;        // heads (MMA M)
+constexpr int kD = 576;        // latent + rope
+constexpr int kDC = 512;       // value columns
+constexpr int kNC = 64;        // selected rows per chunk
+constexpr int kNAmax = 5;      // 128-byte column atoms of the larger half
+constexpr int kQBytes = kNAmax * kH * 128;    // 80 KB
+constexpr int kKVStage = kNAmax * kNC * 128;  // 40 KB
+constexpr int kStages = 2;
+constexpr int kPBytes = kH * kNC * 2;         // 16 KB
+constexpr int kXBytes = kH * kNC * 4;         // 32 KB
+constexpr int kMaxTopK = 2048;
+constexpr int kSmem = kQBytes + kStages * kKVStage + kPBytes + kXBytes + kMaxTopK * 4 + 1024 + 1024;
+constexpr int kTmemCols = 512;                // S0 [0,64) S1 [64,128) O [128,384)
+constexpr int kOCol = 128;
+constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows > 2^8
+
+struct Params {
+  Seqs seqs;
+  int top_k;
+  float scale_log2;  // softmax scale · log2(e)
+  int nsplit;
+  int out_f32;
+  const int32_t* idx;
+  void* out;
+  float* lse;
+  float* part_o;     // [total_q * nsplit * 2][128][256] fp32 (nsplit > 1)
+  float* part_ml;    // [total_q * nsplit * 2][128][2]
+  int* counters;     // [total_q * 2], zero at launch
+  uint32_t* status;
+};
+
+__device__ __forceinline__ bool row_info_noflag(const Seqs& s, int t, int& pos, int& k0) {
+  int lo = 0, hi = s.B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(s.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int q0 = __ldg(s.cu_q + lo), q1 = __ldg(s.cu_q + lo + 1);
+  k0 = __ldg(s.cu_k + lo);
+  const int k1 = __ldg(s.cu_k + lo + 1);
+  const int T = q1 - q0, L = k1 - k0;
+  pos = L - T + (t - q0);
+  return t >= q0 && t < q1 && T <= L && k0 >= 0 && k1 <= s.total_k && L <= s.max_k_len;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
+              Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* qs = smem;
+  uint8_t* kvs = qs + kQBytes;
+  uint8_t* ps = kvs + kStages * kKVStage;
+  float* xs = reinterpret_cast<float*>(ps + kPBytes);
+  int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + kXBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(list + kMaxTopK);
+  uint64_t* kv_full = bars;          // [2]
+  uint64_t* kv_empty = bars + 2;     // [2]
+  uint64_t* s_full = bars + 4;       // [2]
+  uint64_t* s_empty = bars + 6;      // [2]
+  uint64_t* q_full = bars + 8;
+  uint64_t* q_empty = bars + 9;
+  uint64_t* p_full = bars + 10;
+  uint64_t* p_empty = bars + 11;
+  uint64_t* pv_done = bars + 12;
+  uint64_t* x_full = bars + 13;      // peer's 128 softmax threads arrive here
+  uint64_t* x_empty = bars + 14;
+  uint64_t* meta_full = bars + 15;
+  uint64_t* meta_empty = bars + 16;
+  uint64_t* drain = bars + 17;
+  volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 18);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
+  int* s_last = reinterpret_cast<int*>(bars + 21);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int NA = rank ? 5 : 4;                 // column atoms this CTA owns for S
+  const int colbase = rank ? 256 : 0;          // first latent column it owns
+  const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const int nunits = p.seqs.total_q * p.nsplit;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
+    }
+    mbar_init(q_full, 1); mbar_init(q_empty, 1);
+    mbar_init(p_full, 4); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
+    mbar_init(x_full, 128); mbar_init(x_empty, 128);
+    mbar_init(meta_full, 1); mbar_init(meta_empty, 5);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&kvmap);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- producer warp: index compaction + TMA ----------------
+    int gc = 0, qi = 0;
+    for (int u = cluster_id, ui = 0; u < nunits; u += nclusters, ++ui) {
+      const int t = u / p.nsplit, sp = u - t * p.nsplit;
+      int pos = 0, k0 = 0;
+      const bool ok = row_info_noflag(p.seqs, t, pos, k0);
+      if (!mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+      // valid entries of idx[t, :] in slot order -> list (absolute key rows)
+      const int32_t* irow = p.idx + (int64_t)t * p.top_k;
+      int base = 0;
+      for (int i0 = 0; i0 < p.top_k; i0 += 32) {
+        const int i = i0 + lane;
+        const int v = (ok && i < p.top_k) ? __ldg(irow + i) : -1;
+        const bool valid = v >= 0 && v <= pos;
+        if (!valid && v != -1 && sp == 0 && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
+        const unsigned bal = __ballot_sync(0xffffffffu, valid);
+        if (valid) list[base + __popc(bal & ((1u << lane) - 1u))] = k0 + v;
+        base += __popc(bal);
+      }
+      __syncwarp();
+      const int nv = base;
+      if (lane == 0) { *meta_nv = nv; mbar_arrive(meta_full); }
+      const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
+      const int n = hi - lo, nch = (n + kNC - 1) / kNC;
+      if (nch == 0) continue;
+      bool stop = false;
+      if (lane == 0) {
+        if (mbar_wait(q_empty, (qi & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+          mbar_arrive_expect_tx(q_full, NA * kH * 128);
+          for (int a = 0; a < NA; ++a)
+            tma_load_2d(qs + a * (kH * 128), &qmap, q_full, colbase + 64 * a, t * kH);
+        } else {
+          stop = true;
+        }
+      }
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      if (stop) break;
+      ++qi;
+      for (int c = 0; c < nch; ++c, ++gc) {
+        const int st = gc & 1;
+        if (lane == 0) {
+          if (mbar_wait(&kv_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag, p.status,
+                        DSA_FLAG_TIMEOUT))
+            mbar_arrive_expect_tx(&kv_full[st], NA * kNC * 128);
+          else
+            stop = true;
+        }
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop) break;
+        if (lane < kNC / 4) {  // 16 lanes, one 4-row group each
+          int r[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = c * kNC + lane * 4 + i;
+            r[i] = list[lo + (j < n ? j : 0)];
+          }
+          uint8_t* dst = kvs + st * kKVStage + lane * 4 * 128;
+          for (int a = 0; a < NA; ++a)
+            tma_gather4(dst + a * (kNC * 128), &kvmap, &kv_full[st], colbase + 64 * a, r[0], r[1],
+                        r[2], r[3]);
+        }
+        __syncwarp();
+      }
+      if (stop) break;
+    }
+    // every copy issued has landed before the CTA may exit
+    if (lane == 0) {
+      for (int i = (gc > 2 ? gc - 2 : 0); i < gc; ++i) mbar_wait_drain(&kv_full[i & 1], (i >> 1) & 1);
+      if (qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(kH, kNC);                  // K-major A and B
+      const uint32_t idesc_pv = idesc_bf16(kH, 256, false, true);    // V is MN-major
+      const uint32_t q0 = smem_u32(qs), kv0 = smem_u32(kvs), p0 = smem_u32(ps);
+      int gc = 0, qi = 0;
+      bool stop = false;
+      auto pv = [&](int g, int first) -> bool {
+        if (!mbar_wait(p_full, g & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) return false;
+        tc_fence_after();
+        const uint32_t vb = kv0 + (g & 1) * kKVStage;
+#pragma unroll
+        for (int kk = 0; kk < kNC / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(p0 + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kNC * 128, 1024);
+          mma_bf16(tmem + kOCol, ad, bd, idesc_pv, (first == 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kv_empty[g & 1]);
+        mma_commit(p_empty);
+        mma_commit(pv_done);
+        return true;
+      };
+      for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
+        if (!mbar_wait(meta_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+        const int nv = *meta_nv;
+        mbar_arrive(meta_empty);
+        const int t = u / p.nsplit, sp = u - t * p.nsplit;
+        (void)t;
+        const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
+        const int nch = (hi - lo + kNC - 1) / kNC;
+        if (nch == 0) continue;
+        if (!mbar_wait(q_full, qi & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+        tc_fence_after();
+        ++qi;
+        const int g_first = gc;
+        for (int c = 0; c < nch; ++c, ++gc) {
+          const int st = gc & 1;
+          if (!mbar_wait(&kv_full[st], (gc >> 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT) ||
+              !mbar_wait(&s_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag, p.status,
+                         DSA_FLAG_TIMEOUT)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t kb = kv0 + st * kKVStage;
+          for (int a = 0; a < NA; ++a) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(q0 + a * (kH * 128) + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(kb + a * (kNC * 128) + kk * 32, 16, 1024);
+              mma_bf16(tmem + st * kNC, ad, bd, idesc_s, (a | kk) ? 1u : 0u);
+            }
+          }
+          mma_commit(&s_full[st]);
+          if (c == nch - 1) mma_commit(q_empty);
+          if (c > 0 && !pv(gc - 1, gc - 1 == g_first)) { stop = true; break; }
+        }
+        if (stop) break;
+        if (!pv(gc - 1, gc - 1 == g_first)) break;
+      }
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ---------------- softmax / epilogue: one thread per head ----------------
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* xrow = xs + h * kNC;
+    const uint32_t xrow_peer = mapa(smem_u32(xrow), peer);
+    const uint32_t x_full_peer = mapa(smem_u32(x_full), peer);
+    const uint32_t x_empty_peer = mapa(smem_u32(x_empty), peer);
+    uint8_t* prow = ps + h * 128;
+    int gc = 0;
+    bool stop = false;
+    for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
+      if (!mbar_wait(meta_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+      const int nv = *meta_nv;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(meta_empty);
+      const int t = u / p.nsplit, sp = u - t * p.nsplit;
+      const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
+      const int n = hi - lo, nch = (n + kNC - 1) / kNC;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int c = 0; c < nch; ++c, ++gc) {
+        const int sb = gc & 1;
+        const int rows_in = min(kNC, n - c * kNC);
+        if (!mbar_wait(&s_full[sb], (gc >> 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+          stop = true; break;
+        }
+        tc_fence_after();
+        float s[kNC];
+        {
+          uint32_t r[32];
+          tmem_ld32(lane_base + sb * kNC, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+          tmem_ld32(lane_base + sb * kNC + 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[sb]);
+        // exchange the partial logits with the peer CTA
+        if (!mbar_wait_cluster(x_empty, (gc & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+          stop = true; break;
+        }
+#pragma unroll
+        for (int q = 0; q < kNC / 4; ++q)
+          reinterpret_cast<float4*>(xrow)[q ^ (h & 15)] =
+              make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
+        mbar_arrive_remote(x_full_peer);
+        if (!mbar_wait_cluster(x_full, gc & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+          stop = true; break;
+        }
+        float m_c = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kNC / 4; ++q) {
+          const float4 o = ld_cluster_f4(xrow_peer + (uint32_t)((q ^ (h & 15)) * 16));
+          const float other[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * q + e;
+            const float lo_part = rank ? other[e] : s[i];
+            const float hi_part = rank ? s[i] : other[e];
+            const float x = (lo_part + hi_part) * p.scale_log2;
+            s[i] = i < rows_in ? x : -INFINITY;
+            m_c = fmaxf(m_c, s[i]);
+          }
+        }
+        mbar_arrive_remote(x_empty_peer);
+        // running max: move the reference only when it grows by more than 2^8
+        const bool grow = m_c > m_ref + kRescaleLog2;
+        const float m_new = grow ? m_c : m_ref;
+        const float factor = grow ? exp2f(m_ref - m_new) : 1.f;
+        l *= factor;
+        if (__any_sync(0xffffffffu, grow && c > 0)) {
+          if (!mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+            stop = true; break;
+          }
+          tc_fence_after();
+          for (int b = 0; b < 8; ++b) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + kOCol + 32 * b, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * factor);
+            tmem_st32(lane_base + kOCol + 32 * b, r);
+          }
+          tc_fence_before();
+        }
+        m_ref = m_new;
+        uint32_t pk[kNC / 2];
+#pragma unroll
+        for (int i = 0; i < kNC / 2; ++i) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(s[2 * i] - m_ref),
+                                                          exp2f(s[2 * i + 1] - m_ref));
+          const float2 f2 = __bfloat1622float2(b2);
+          l += f2.x + f2.y;
+          pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        if (!mbar_wait(p_empty, (gc & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+          stop = true; break;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(prow + ((j ^ (h & 7)) * 16)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (stop) break;
+
+      // ---- epilogue of the unit ----
+      const bool have = nch > 0;
+      if (have) {
+        if (!mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+        tc_fence_after();
+      }
+      if (p.nsplit == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t obase = ((int64_t)t * kH + h) * kDC + colbase;
+        for (int b = 0; b < 8; ++b) {
+          uint32_t r[32];
+          if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          if (p.out_f32) {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + 32 * b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                 __uint_as_float(r[4 * i + 2]) * inv,
+                                 __uint_as_float(r[4 * i + 3]) * inv);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + 32 * b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
+                                          __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
+                w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+        if (rank == 0 && p.lse)
+          p.lse[(int64_t)t * kH + h] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      } else {
+        // split of a row: publish (O, m, l); the last split of the row merges them
+        const int64_t slot = ((int64_t)t * p.nsplit + sp) * 2 + rank;
+        float* po = p.part_o + (slot * kH + h) * 256;
+        for (int b = 0; b < 8; ++b) {
+          uint32_t r[32];
+          if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(po + 32 * b)[i] =
+                make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        }
+        p.part_ml[(slot * kH + h) * 2] = m_ref;
+        p.part_ml[(slot * kH + h) * 2 + 1] = l;
+        __threadfence();
+        named_bar(1, 128);
+        if (threadIdx.x == 64) *s_last = atomicAdd(p.counters + t * 2 + rank, 1) == p.nsplit - 1;
+        named_bar(1, 128);
+        if (*s_last) {
+          __threadfence();
+          float M = -INFINITY;
+          for (int s2 = 0; s2 < p.nsplit; ++s2) {
+            const int64_t sl = ((int64_t)t * p.nsplit + s2) * 2 + rank;
+            M = fmaxf(M, __ldcg(p.part_ml + (sl * kH + h) * 2));
+          }
+          float wsum = 0.f, wt[4];
+          for (int s2 = 0; s2 < p.nsplit; ++s2) {
+            const int64_t sl = ((int64_t)t * p.nsplit + s2) * 2 + rank;
+            const float ms = __ldcg(p.part_ml + (sl * kH + h) * 2);
+            const float ls = __ldcg(p.part_ml + (sl * kH + h) * 2 + 1);
+            wt[s2] = ls > 0.f ? exp2f(ms - M) : 0.f;
+            wsum += wt[s2] * ls;
+          }
+          const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+          const int64_t obase = ((int64_t)t * kH + h) * kDC + colbase;
+          for (int c4 = 0; c4 < 64; ++c4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s2 = 0; s2 < p.nsplit; ++s2) {
+              const int64_t sl = ((int64_t)t * p.nsplit + s2) * 2 + rank;
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sl * kH + h) * 256) + c4);
+              acc.x += wt[s2] * v.x; acc.y += wt[s2] * v.y; acc.z += wt[s2] * v.z; acc.w += wt[s2] * v.w;
+            }
+            if (p.out_f32) {
+              reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase)[c4] =
+                  make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            } else {
+              const __nv_bfloat162 a2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+              reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + obase)[c4] =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&a2),
+                             *reinterpret_cast<const uint32_t*>(&b2));
+            }
+          }
+          if (rank == 0 && p.lse)
+            p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f
+                                                    : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while its peer may still touch its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool sfa_tc_eligible(const SfaArgs& a) {
+  return a.kv_dtype == DSA_BF16 && a.h == kH && a.d_c == kDC && a.d_rope == kD - kDC &&
+         a.top_k <= kMaxTopK;
+}
+
+int sfa_tc_nsplit(int total_q) {
+  if (total_q <= 0) return 1;
+  int s = num_sms() / (2 * total_q);
+  return s < 1 ? 1 : (s > 4 ? 4 : s);
+}
+
+size_t sfa_tc_scratch_bytes(int total_q) {
+  const int ns = sfa_tc_nsplit(total_q);
+  if (ns == 1) return 0;
+  const size_t slots = (size_t)total_q * ns * 2;
+  return align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256) +
+         align_up((size_t)total_q * 2 * 4, 256);
+}
+
+int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
+  if (a.seqs.total_q == 0) return DSA_OK;
+  const int ns = sfa_tc_nsplit(a.seqs.total_q);
+  CUtensorMap qmap, kvmap;
+  int rc = make_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD,
+                        (uint64_t)a.seqs.total_q * kH, kD * 2, 64, kH);
+  if (rc != DSA_OK) return rc;
+  rc = make_tmap_2d(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kD, (uint64_t)a.seqs.total_k,
+                    kD * 2, 64, 1);
+  if (rc != DSA_OK) return rc;
+  Params p{};
+  p.seqs = a.seqs;
+  p.top_k = a.top_k;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.nsplit = ns;
+  p.out_f32 = a.out_dtype == DSA_F32;
+  p.idx = a.idx;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.status = a.status;
+  if (ns > 1) {
+    const size_t slots = (size_t)a.seqs.total_q * ns * 2;
+    char* b = static_cast<char*>(scratch);
+    p.part_o = reinterpret_cast<float*>(b);
+    b += align_up(slots * kH * 256 * 4, 256);
+    p.part_ml = reinterpret_cast<float*>(b);
+    b += align_up(slots * kH * 2 * 4, 256);
+    p.counters = reinterpret_cast<int*>(b);
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, (size_t)a.seqs.total_q * 2 * 4, stream);
+    if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
+  }
+  if (cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+      cudaSuccess)
+    return check_launch("sfa_tc: smem attribute");
+  const int64_t units = (int64_t)a.seqs.total_q * ns;
+  const int max_clusters = num_sms() / 2;
+  const int clusters = (int)(units < max_clusters ? units : max_clusters);
+  DSA_LAUNCH("sfa_tc", stream, sfa_tc_kernel<<<2 * clusters, 192, kSmem, stream>>>(qmap, kvmap, p));
+  return check_launch("sfa_tc");
+}
+
+}  // namespace dsa

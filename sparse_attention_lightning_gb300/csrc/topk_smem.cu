@@ -78,8 +78,30 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   }
 
   // --- load the row as keys, with its min and max ----------------------------
+  // Vector loads, several in flight per thread (the row usually sits in L2).
   uint32_t lmin = 0xffffffffu, lmax = 0u;
-  for (int i = tid; i < n; i += kT) {
+  int head = (int)(((16u - ((uintptr_t)row & 15u)) & 15u) >> 2);  // scalars before 16-B alignment
+  if (((uintptr_t)row & 3u) != 0) head = n;                          // not even 4-B aligned
+  head = min(head, n);
+  for (int i = tid; i < head; i += kT) {
+    const uint32_t key = order_key(row[i]);
+    keys[i] = key;
+    lmin = min(lmin, key);
+    lmax = max(lmax, key);
+  }
+  const int nvec = (n - head) >> 2;
+  const float4* rv = reinterpret_cast<const float4*>(row + head);
+#pragma unroll 4
+  for (int v = tid; v < nvec; v += kT) {
+    const float4 f = __ldcg(rv + v);
+    const int i = head + 4 * v;
+    const uint32_t k0 = order_key(f.x), k1 = order_key(f.y), k2 = order_key(f.z),
+                   k3 = order_key(f.w);
+    keys[i] = k0; keys[i + 1] = k1; keys[i + 2] = k2; keys[i + 3] = k3;
+    lmin = min(min(lmin, min(k0, k1)), min(k2, k3));
+    lmax = max(max(lmax, max(k0, k1)), max(k2, k3));
+  }
+  for (int i = head + 4 * nvec + tid; i < n; i += kT) {
     const uint32_t key = order_key(row[i]);
     keys[i] = key;
     lmin = min(lmin, key);

@@ -157,6 +157,44 @@ def test_sfa_flags_bad_indices_and_skips_them():
     assert ws.status() == 0
 
 
+@pytest.mark.parametrize("nq,out_dtype", [(3, "bf16"), (90, "bf16"), (5, "f32")])
+def test_tensor_core_sfa_standalone(nq, out_dtype):
+    # H = 128, d_c = 512, d_rope = 64 runs on tcgen05 CTA pairs; few queries split each row
+    # over several clusters (merged by the last one), many queries do not.  Index rows mix
+    # valid positions, -1 padding anywhere, out-of-range entries and a repeated entry.
+    L = 3000
+    cfg = W.custom([nq], [L], h_idx=4, d_idx=32, h=128, d_c=512, d_rope=64, top_k=2048,
+                   idx_dtype="bf16", kv_dtype="bf16", out_dtype=out_dtype)
+    case = W.make_case(cfg, seed=41)
+    d = to_dev(case)
+    P = problem(case, d)
+    g = torch.Generator().manual_seed(nq)
+    idx = torch.full((nq, 2048), -1, dtype=torch.int32)
+    counts = []
+    for t in range(nq):
+        pos = L - nq + t
+        n = [2048, 1, 65, 700, 2047][t % 5]
+        sel = torch.randperm(pos + 1, generator=g)[:n].to(torch.int32)
+        slots = torch.randperm(2048, generator=g)[:sel.numel()]
+        idx[t, slots] = sel
+        counts.append(sel.numel())
+    idx[0, 5] = idx[0, 6]                # a repeated entry counts twice
+    idx[1, 7] = L + 5                    # out of range: flagged and skipped
+    ws = dsa.Workspace()
+    ws.clear_status()
+    out, lse = dsa.sparse_mla_attn(P, d["q"], d["kv"], idx.cuda(), ws=ws)
+    flags = ws.status()
+    assert flags == 0x1, hex(flags)
+    p = O.problem_from_case(case)
+    idn = idx.numpy()
+    for t in range(nq):
+        pos = L - nq + t
+        row = idn[t]
+        valid = row[(row >= 0) & (row <= pos)]
+        ref_out, ref_lse = p.sfa(t, valid)
+        check_attn_row(to_np(out)[t], to_np(lse)[t], ref_out, ref_lse, tol_for(cfg), f"row {t}")
+
+
 def test_repeat_runs_are_bitwise_identical():
     cfg = W.custom([1, 1], [3000, 2500], h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64,
                    top_k=2048, idx_dtype="bf16", kv_dtype="bf16")
