@@ -77,7 +77,8 @@ def work_model(cfg):
 
 # Which stage each library kernel belongs to (for the roofline of the dominant kernel).
 KERNEL_STAGE = {
-    "indexer_scores_simt": "indexer", "topk_rows": "topk", "sfa_simt": "sfa",
+    "indexer_scores_simt": "indexer", "indexer_tc_bf16": "indexer", "indexer_tc_fp8": "indexer",
+    "topk_rows": "topk", "topk_smem": "topk", "sfa_simt": "sfa", "sfa_tc": "sfa",
 }
 
 

@@ -30,8 +30,8 @@
 // P = exp2(x - m) as bf16 into shared memory; O += P · V (M=128, N=256, K=64,
 // V read MN-major straight from the gathered tile).
 //
-// Decode rows are split over 2-4 clusters when there are few queries; the last
-// cluster of a row to finish merges the partial (O, max, sum) of the others.
+// Decode rows are split over 2 clusters when there are few queries; the second
+// cluster of a row to finish merges the other's partial (O, max, sum) into its own.
 // Every wait is bounded (DSA_FLAG_TIMEOUT).
 #include "dsa_internal.cuh"
 #include "tc_sm100.cuh"
@@ -110,11 +110,11 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
   uint64_t* x_empty = bars + 14;
   uint64_t* meta_full = bars + 15;
   uint64_t* meta_empty = bars + 16;
-  uint64_t* drain = bars + 17;
-  volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 18);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
-  int* s_last = reinterpret_cast<int*>(bars + 21);
+  uint64_t* drain = bars + 17;      // [2]: MMA drain, merge copy
+  volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 19);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+  int* s_last = reinterpret_cast<int*>(bars + 22);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -134,6 +134,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     mbar_init(x_full, 128); mbar_init(x_empty, 128);
     mbar_init(meta_full, 1); mbar_init(meta_empty, 5);
     mbar_init(drain, 1);
+    mbar_init(drain + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&qmap);
@@ -153,20 +154,36 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
       int pos = 0, k0 = 0;
       const bool ok = row_info_noflag(p.seqs, t, pos, k0);
       if (!mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
-      // valid entries of idx[t, :] in slot order -> list (absolute key rows)
+      // valid entries of idx[t, :] in slot order -> list (absolute key rows).  Each lane
+      // owns a contiguous run of up to 64 slots, loaded all at once (independent loads).
       const int32_t* irow = p.idx + (int64_t)t * p.top_k;
-      int base = 0;
-      for (int i0 = 0; i0 < p.top_k; i0 += 32) {
-        const int i = i0 + lane;
-        const int v = (ok && i < p.top_k) ? __ldg(irow + i) : -1;
-        const bool valid = v >= 0 && v <= pos;
-        if (!valid && v != -1 && sp == 0 && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
-        const unsigned bal = __ballot_sync(0xffffffffu, valid);
-        if (valid) list[base + __popc(bal & ((1u << lane) - 1u))] = k0 + v;
-        base += __popc(bal);
+      const int seg = (p.top_k + 31) / 32;
+      const int s0 = lane * seg;
+      int v[kMaxTopK / 32];
+#pragma unroll
+      for (int j = 0; j < kMaxTopK / 32; ++j)
+        v[j] = (ok && j < seg && s0 + j < p.top_k) ? __ldg(irow + s0 + j) : -1;
+      int cnt = 0;
+      bool bad = false;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK / 32; ++j) {
+        const bool valid = v[j] >= 0 && v[j] <= pos;
+        bad |= !valid && v[j] != -1;
+        cnt += valid;
       }
+      if (bad && sp == 0 && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
+      int before = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, before, o);
+        if (lane >= o) before += y;
+      }
+      const int nv = __shfl_sync(0xffffffffu, before, 31);
+      before -= cnt;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK / 32; ++j)
+        if (v[j] >= 0 && v[j] <= pos) list[before++] = k0 + v[j];
       __syncwarp();
-      const int nv = base;
       if (lane == 0) { *meta_nv = nv; mbar_arrive(meta_full); }
       const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
       const int n = hi - lo, nch = (n + kNC - 1) / kNC;
@@ -451,38 +468,59 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         if (threadIdx.x == 64) *s_last = atomicAdd(p.counters + t * 2 + rank, 1) == p.nsplit - 1;
         named_bar(1, 128);
         if (*s_last) {
+          // The other split's (O, m, l) of this column half: one bulk copy of its
+          // 128 KB into the (now idle) query/KV area, then each thread merges its head row.
           __threadfence();
-          float M = -INFINITY;
-          for (int s2 = 0; s2 < p.nsplit; ++s2) {
-            const int64_t sl = ((int64_t)t * p.nsplit + s2) * 2 + rank;
-            M = fmaxf(M, __ldcg(p.part_ml + (sl * kH + h) * 2));
+          const int64_t other = ((int64_t)t * p.nsplit + (1 - sp)) * 2 + rank;
+          float* po2 = reinterpret_cast<float*>(qs);
+          if (threadIdx.x == 64) {
+            fence_proxy_async_all();
+            mbar_arrive_expect_tx(drain + 1, kH * 256 * 4);
+            for (int c = 0; c < 8; ++c)
+              bulk_load(po2 + c * 4096, p.part_o + (other * kH) * 256 + c * 4096, 16384, drain + 1);
           }
-          float wsum = 0.f, wt[4];
-          for (int s2 = 0; s2 < p.nsplit; ++s2) {
-            const int64_t sl = ((int64_t)t * p.nsplit + s2) * 2 + rank;
-            const float ms = __ldcg(p.part_ml + (sl * kH + h) * 2);
-            const float ls = __ldcg(p.part_ml + (sl * kH + h) * 2 + 1);
-            wt[s2] = ls > 0.f ? exp2f(ms - M) : 0.f;
-            wsum += wt[s2] * ls;
-          }
+          const float mo = __ldcg(p.part_ml + (other * kH + h) * 2);
+          const float lo2 = __ldcg(p.part_ml + (other * kH + h) * 2 + 1);
+          const float M = fmaxf(m_ref, mo);
+          const float wa = l > 0.f ? exp2f(m_ref - M) : 0.f;
+          const float wb = lo2 > 0.f ? exp2f(mo - M) : 0.f;
+          const float wsum = wa * l + wb * lo2;
           const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+          if (!mbar_wait(drain + 1, 0, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+          const float* orow = po2 + h * 256;
           const int64_t obase = ((int64_t)t * kH + h) * kDC + colbase;
-          for (int c4 = 0; c4 < 64; ++c4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s2 = 0; s2 < p.nsplit; ++s2) {
-              const int64_t sl = ((int64_t)t * p.nsplit + s2) * 2 + rank;
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sl * kH + h) * 256) + c4);
-              acc.x += wt[s2] * v.x; acc.y += wt[s2] * v.y; acc.z += wt[s2] * v.z; acc.w += wt[s2] * v.w;
+          for (int b = 0; b < 8; ++b) {
+            uint32_t r[32];
+            if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
+            else
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = 0u;
+            float res[32];
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq) {
+              const float4 o = reinterpret_cast<const float4*>(orow + 32 * b)[qq];
+              res[4 * qq] = (wa * __uint_as_float(r[4 * qq]) + wb * o.x) * inv;
+              res[4 * qq + 1] = (wa * __uint_as_float(r[4 * qq + 1]) + wb * o.y) * inv;
+              res[4 * qq + 2] = (wa * __uint_as_float(r[4 * qq + 2]) + wb * o.z) * inv;
+              res[4 * qq + 3] = (wa * __uint_as_float(r[4 * qq + 3]) + wb * o.w) * inv;
             }
             if (p.out_f32) {
-              reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase)[c4] =
-                  make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+              float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + 32 * b);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                o[i] = make_float4(res[4 * i], res[4 * i + 1], res[4 * i + 2], res[4 * i + 3]);
             } else {
-              const __nv_bfloat162 a2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-              reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + obase)[c4] =
-                  make_uint2(*reinterpret_cast<const uint32_t*>(&a2),
-                             *reinterpret_cast<const uint32_t*>(&b2));
+              uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + 32 * b);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(res[8 * i + 2 * e], res[8 * i + 2 * e + 1]);
+                  w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
             }
           }
           if (rank == 0 && p.lse)
@@ -510,8 +548,7 @@ bool sfa_tc_eligible(const SfaArgs& a) {
 
 int sfa_tc_nsplit(int total_q) {
   if (total_q <= 0) return 1;
-  int s = num_sms() / (2 * total_q);
-  return s < 1 ? 1 : (s > 4 ? 4 : s);
+  return num_sms() >= 4 * total_q ? 2 : 1;
 }
 
 size_t sfa_tc_scratch_bytes(int total_q) {

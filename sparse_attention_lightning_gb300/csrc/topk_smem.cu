@@ -7,10 +7,11 @@
 // the smaller position, written in ascending position order, -1 padded.
 //
 // The row is read once from global memory into shared memory as
-// order-preserving uint32 keys, with its min and max.  Radix digits start just
-// below the bits all keys share (so the first 8-bit digit already spreads the
-// row over up to 256 bins), with per-warp histograms to keep shared-memory
-// atomics uncontended.  Once the keys still in play fit a small buffer they
+// order-preserving uint32 keys, with its min and max.  The radix select runs on
+// the offsets v = key - min, whose top 8 significant bits already spread the
+// row over up to 256 bins (on raw keys the first digit would be the float
+// exponent, shared by almost every score), with per-warp histograms to keep
+// shared-memory atomics uncontended.  Once the keys still in play fit a small buffer they
 // are compacted and later digits scan only them.  A single block-wide prefix
 // sum then places every selected position: each thread owns a contiguous run
 // of keys, read in a lane-rotated order so the 32 lanes never share a bank.
@@ -115,11 +116,12 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   for (int w = 1; w < kW; ++w) { kmin = min(kmin, red_min[w]); kmax = max(kmax, red_max[w]); }
 
   // --- radix select of the exact n-th largest key -------------------------------
-  uint32_t prefix = kmax, need = (uint32_t)k;
+  // on offsets v = key - kmin in [0, kmax - kmin]; T = kmin + (selected offset)
+  uint32_t prefix = kmax - kmin, need = (uint32_t)k;
   if (kmin != kmax) {
-    int hb = 31 - __clz(kmax ^ kmin);                     // highest bit that differs
-    uint32_t mask = hb == 31 ? 0u : ~((2u << hb) - 1u);   // bits shared by every key
-    prefix = kmax & mask;
+    int hb = 31 - __clz(kmax - kmin);                     // highest bit any offset uses
+    uint32_t mask = hb == 31 ? 0u : ~((2u << hb) - 1u);   // bits zero in every offset
+    prefix = 0u;
     const uint32_t* src = keys;
     int src_n = n;
     bool compacted = false;
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
       __syncthreads();
       uint32_t* h = hist + warp * 256;
       for (int i = tid; i < src_n; i += kT) {
-        const uint32_t key = src[i];
-        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & dmask], 1u);
+        const uint32_t v = src[i] - kmin;
+        if ((v & mask) == prefix) atomicAdd(&h[(v >> shift) & dmask], 1u);
       }
       __syncthreads();
       if (tid < 256) {
@@ -177,9 +179,15 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
       if (!compacted && cnt <= (uint32_t)kCandCap) {
         if (tid == 0) s_ncand = 0;
         __syncthreads();
-        for (int i = tid; i < n; i += kT) {
-          const uint32_t key = keys[i];
-          if ((key & mask) == prefix) cand[atomicAdd(&s_ncand, 1u)] = key;
+        for (int i0 = 0; i0 < n; i0 += kT) {  // one counter update per warp
+          const int i = i0 + tid;
+          const uint32_t key = i < n ? keys[i] : 0u;
+          const bool hitk = i < n && ((key - kmin) & mask) == prefix;
+          const unsigned bal = __ballot_sync(0xffffffffu, hitk);
+          uint32_t wbase = 0;
+          if (lane == 0 && bal) wbase = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
+          wbase = __shfl_sync(0xffffffffu, wbase, 0);
+          if (hitk) cand[wbase + __popc(bal & ((1u << lane) - 1u))] = key;
         }
         __syncthreads();
         src = cand;
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
       }
     }
   }
-  const uint32_t T = prefix;  // the n-th largest key; `need` of the keys equal to it are kept
+  const uint32_t T = kmin + prefix;  // the n-th largest key; `need` of the keys equal to it are kept
 
   // --- ordered write -------------------------------------------------------------------
   const int m = (n + 32 * kT - 1) / (32 * kT);  // 32-key chunks per thread
