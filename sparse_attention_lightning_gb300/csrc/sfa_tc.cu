@@ -22,13 +22,17 @@
 // own 256 value columns: O_half (128 x 256 fp32) lives in TMEM next to a
 // double-buffered 128 x 64 S tile.
 //
-// Per chunk of 64 selected rows: TMA tile::gather4 loads (4 rows x 128 B per
-// instruction, 128-byte swizzle) into a 2-stage ring; S = Q_half · KV_half^T
-// (M=128, N=64, K=256|320, K-major operands); the softmax warps (one thread per
-// head) read S from TMEM, exchange halves with the peer CTA, keep a running max
-// (the output is rescaled only when the max grows by more than 2^8), write
-// P = exp2(x - m) as bf16 into shared memory; O += P · V (M=128, N=256, K=64,
-// V read MN-major straight from the gathered tile).
+// Per chunk of 64 selected rows:
+//  * producer warp: the 16-byte pieces of the CTA's columns of the 64 rows go
+//    straight into the 128-byte-swizzled operand layout with cp.async (one warp
+//    instruction moves 4 rows x 128 B); completion arrives on an mbarrier;
+//  * MMA thread: S = Q_half · KV_half^T (M=128, N=64, K=256|320, K-major), then,
+//    once P is ready, O += P · V (M=128, N=256, K=64, V read MN-major straight
+//    from the gathered tile);
+//  * softmax warps (one thread per head): read S from TMEM, push their partial
+//    into the peer CTA's shared memory (coalesced remote stores), read the
+//    peer's from their own, keep a running max (O is rescaled only when the max
+//    grows by more than 2^8), write P = 2^(x - m) as bf16 for the PV MMA.
 //
 // Decode rows are split over 2 clusters when there are few queries; the second
 // cluster of a row to finish merges the other's partial (O, max, sum) into its own.
@@ -64,40 +68,97 @@ struct Params {
   int nsplit;
   int out_f32;
   const int32_t* idx;
+  const __nv_bfloat16* kv;
   void* out;
   float* lse;
-  float* part_o;     // [total_q * nsplit * 2][128][256] fp32 (nsplit > 1)
+  float4* part_o;    // [total_q * nsplit * 2][64][128] float4 (nsplit > 1)
   float* part_ml;    // [total_q * nsplit * 2][128][2]
   int* counters;     // [total_q * 2], zero at launch
   uint32_t* status;
 };
 
-__device__ __forceinline__ bool row_info_noflag(const Seqs& s, int t, int& pos, int& k0) {
-  int lo = 0, hi = s.B - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(s.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Sequence of packed query row t, by a 32-way search over cu_q (whole warp).
+__device__ __forceinline__ int seq_of_row(const Seqs& s, int t, int lane) {
+  int lo = 0, hi = s.B;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int probe = lo + lane * step;
+    const int v = probe < hi ? __ldg(s.cu_q + probe) : INT_MAX;
+    const unsigned bal = __ballot_sync(0xffffffffu, v <= t);
+    const int m = 31 - __clz(bal);  // last probe at or below t (probe 0 always is)
+    lo = lo + m * step;
+    hi = min(hi, lo + step);
   }
-  const int q0 = __ldg(s.cu_q + lo), q1 = __ldg(s.cu_q + lo + 1);
-  k0 = __ldg(s.cu_k + lo);
-  const int k1 = __ldg(s.cu_k + lo + 1);
-  const int T = q1 - q0, L = k1 - k0;
-  pos = L - T + (t - q0);
-  return t >= q0 && t < q1 && T <= L && k0 >= 0 && k1 <= s.total_k && L <= s.max_k_len;
+  return lo;
+}
+
+// Output of 32 consecutive columns of every head of a warp, staged through
+// shared memory so each store instruction writes whole row segments.
+__device__ __forceinline__ void store_block(const float (&v)[32], int out_f32, void* out,
+                                            int64_t row0, int col0, uint8_t* stage, int lane) {
+  if (out_f32) {  // 32 rows x 128 B
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(stage + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = i * 4 + (lane >> 3), j = lane & 7;
+      const float4 x = *reinterpret_cast<const float4*>(stage + r * 128 + ((j ^ (r & 7)) * 16));
+      reinterpret_cast<float4*>(static_cast<float*>(out) + (row0 + r) * kDC + col0)[j] = x;
+    }
+  } else {        // 32 rows x 64 B
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(stage + lane * 64 + ((j ^ (lane & 3)) * 16)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2), j = lane & 3;
+      const uint4 x = *reinterpret_cast<const uint4*>(stage + r * 64 + ((j ^ (r & 3)) * 16));
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + (row0 + r) * kDC + col0)[j] = x;
+    }
+  }
+  __syncwarp();
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
-              Params p) {
+sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* qs = smem;
   uint8_t* kvs = qs + kQBytes;
   uint8_t* ps = kvs + kStages * kKVStage;
-  float* xs = reinterpret_cast<float*>(ps + kPBytes);
+  float4* xs = reinterpret_cast<float4*>(ps + kPBytes);  // [16][128]: peer's partial logits
   int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + kXBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(list + kMaxTopK);
-  uint64_t* kv_full = bars;          // [2]
+  uint64_t* kv_full = bars;          // [2]  32 producer lanes (cp.async completion)
   uint64_t* kv_empty = bars + 2;     // [2]
   uint64_t* s_full = bars + 4;       // [2]
   uint64_t* s_empty = bars + 6;      // [2]
@@ -110,11 +171,13 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
   uint64_t* x_empty = bars + 14;
   uint64_t* meta_full = bars + 15;
   uint64_t* meta_empty = bars + 16;
-  uint64_t* drain = bars + 17;      // [2]: MMA drain, merge copy
+  uint64_t* drain = bars + 17;       // [2]: MMA drain, merge copy
   volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 19);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
   int* s_last = reinterpret_cast<int*>(bars + 22);
+  uint64_t* sync_a = bars + 23;      // 128 softmax threads: partials written
+  uint64_t* sync_b = bars + 24;      // the arrival count has been taken
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -126,7 +189,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_full[i], 32); mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
     }
     mbar_init(q_full, 1); mbar_init(q_empty, 1);
@@ -135,10 +198,11 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     mbar_init(meta_full, 1); mbar_init(meta_empty, 5);
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
+    mbar_init(sync_a, 128);
+    mbar_init(sync_b, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&qmap);
-    prefetch_tmap(&kvmap);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
   tc_fence_before();
@@ -147,13 +211,38 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- producer warp: index compaction + TMA ----------------
+    // ---------------- producer warp: query block, index compaction, gathers ----------------
     int gc = 0, qi = 0;
-    for (int u = cluster_id, ui = 0; u < nunits; u += nclusters, ++ui) {
+    bool stop = false;
+    for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
       const int t = u / p.nsplit, sp = u - t * p.nsplit;
-      int pos = 0, k0 = 0;
-      const bool ok = row_info_noflag(p.seqs, t, pos, k0);
-      if (!mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+      // the query block needs only t: issue it first
+      if (lane == 0) {
+        if (mbar_wait(q_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+          mbar_arrive_expect_tx(q_full, NA * kH * 128);
+          for (int a = 0; a < NA; ++a)
+            tma_load_2d(qs + a * (kH * 128), &qmap, q_full, colbase + 64 * a, t * kH);
+        } else {
+          stop = true;
+        }
+      }
+      qi = ui + 1;
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      // its sequence and position
+      const int b = seq_of_row(p.seqs, t, lane);
+      int q0 = 0, q1 = 0, k0 = 0, k1 = 0;
+      if (lane == 0) {
+        q0 = __ldg(p.seqs.cu_q + b); q1 = __ldg(p.seqs.cu_q + b + 1);
+        k0 = __ldg(p.seqs.cu_k + b); k1 = __ldg(p.seqs.cu_k + b + 1);
+      }
+      q0 = __shfl_sync(0xffffffffu, q0, 0); q1 = __shfl_sync(0xffffffffu, q1, 0);
+      k0 = __shfl_sync(0xffffffffu, k0, 0); k1 = __shfl_sync(0xffffffffu, k1, 0);
+      const int pos = (k1 - k0) - (q1 - q0) + (t - q0);
+      const bool ok = t >= q0 && t < q1 && q1 - q0 <= k1 - k0 && k0 >= 0 &&
+                      k1 <= p.seqs.total_k && k1 - k0 <= p.seqs.max_k_len;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)))
+        break;
       // valid entries of idx[t, :] in slot order -> list (absolute key rows).  Each lane
       // owns a contiguous run of up to 64 slots, loaded all at once (independent loads).
       const int32_t* irow = p.idx + (int64_t)t * p.top_k;
@@ -187,59 +276,40 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
       if (lane == 0) { *meta_nv = nv; mbar_arrive(meta_full); }
       const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
       const int n = hi - lo, nch = (n + kNC - 1) / kNC;
-      if (nch == 0) continue;
-      bool stop = false;
-      if (lane == 0) {
-        if (mbar_wait(q_empty, (qi & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
-          mbar_arrive_expect_tx(q_full, NA * kH * 128);
-          for (int a = 0; a < NA; ++a)
-            tma_load_2d(qs + a * (kH * 128), &qmap, q_full, colbase + 64 * a, t * kH);
-        } else {
-          stop = true;
-        }
-      }
-      stop = __shfl_sync(0xffffffffu, stop, 0);
-      if (stop) break;
-      ++qi;
+      // gathers: lane = (row sub-index r4 = lane / 8, 16-byte piece j = lane % 8)
+      const int r4 = lane >> 3, jp = lane & 7;
       for (int c = 0; c < nch; ++c, ++gc) {
         const int st = gc & 1;
-        if (lane == 0) {
-          if (mbar_wait(&kv_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag, p.status,
-                        DSA_FLAG_TIMEOUT))
-            mbar_arrive_expect_tx(&kv_full[st], NA * kNC * 128);
-          else
-            stop = true;
-        }
-        stop = __shfl_sync(0xffffffffu, stop, 0);
-        if (stop) break;
-        if (lane < kNC / 4) {  // 16 lanes, one 4-row group each
-          int r[4];
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag,
+                                               p.status, DSA_FLAG_TIMEOUT))) { stop = true; break; }
+        int rowid[kNC / 4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = c * kNC + lane * 4 + i;
-            r[i] = list[lo + (j < n ? j : 0)];
-          }
-          uint8_t* dst = kvs + st * kKVStage + lane * 4 * 128;
-          for (int a = 0; a < NA; ++a)
-            tma_gather4(dst + a * (kNC * 128), &kvmap, &kv_full[st], colbase + 64 * a, r[0], r[1],
-                        r[2], r[3]);
+        for (int g = 0; g < kNC / 4; ++g) {
+          const int jj = c * kNC + g * 4 + r4;
+          rowid[g] = list[lo + (jj < n ? jj : 0)];
         }
-        __syncwarp();
+        const uint32_t dst0 = smem_u32(kvs + st * kKVStage);
+        for (int a = 0; a < NA; ++a) {
+#pragma unroll
+          for (int g = 0; g < kNC / 4; ++g) {
+            const int r = g * 4 + r4;
+            const __nv_bfloat16* src = p.kv + (int64_t)rowid[g] * kD + colbase + a * 64 + jp * 8;
+            cp_async16(dst0 + a * (kNC * 128) + r * 128 + ((jp ^ (r & 7)) * 16), src);
+          }
+        }
+        cp_async_arrive_noinc(&kv_full[st]);
       }
-      if (stop) break;
     }
     // every copy issued has landed before the CTA may exit
-    if (lane == 0) {
-      for (int i = (gc > 2 ? gc - 2 : 0); i < gc; ++i) mbar_wait_drain(&kv_full[i & 1], (i >> 1) & 1);
-      if (qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
-    }
+    cp_async_wait_all();
+    if (lane == 0 && qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(kH, kNC);                  // K-major A and B
       const uint32_t idesc_pv = idesc_bf16(kH, 256, false, true);    // V is MN-major
-      const uint32_t q0 = smem_u32(qs), kv0 = smem_u32(kvs), p0 = smem_u32(ps);
-      int gc = 0, qi = 0;
+      const uint32_t qa = smem_u32(qs), kv0 = smem_u32(kvs), p0 = smem_u32(ps);
+      int gc = 0;
       bool stop = false;
       auto pv = [&](int g, int first) -> bool {
         if (!mbar_wait(p_full, g & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) return false;
@@ -264,22 +334,22 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         (void)t;
         const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
         const int nch = (hi - lo + kNC - 1) / kNC;
-        if (nch == 0) continue;
-        if (!mbar_wait(q_full, qi & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+        if (!mbar_wait(q_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         tc_fence_after();
-        ++qi;
+        if (nch == 0) { mma_commit(q_empty); continue; }
         const int g_first = gc;
         for (int c = 0; c < nch; ++c, ++gc) {
           const int st = gc & 1;
           if (!mbar_wait(&kv_full[st], (gc >> 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT) ||
               !mbar_wait(&s_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag, p.status,
                          DSA_FLAG_TIMEOUT)) { stop = true; break; }
+          fence_proxy_async_smem();  // the cp.async writes, seen by the tensor core
           tc_fence_after();
           const uint32_t kb = kv0 + st * kKVStage;
           for (int a = 0; a < NA; ++a) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(q0 + a * (kH * 128) + kk * 32, 16, 1024);
+              const uint64_t ad = sdesc_sw128(qa + a * (kH * 128) + kk * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(kb + a * (kNC * 128) + kk * 32, 16, 1024);
               mma_bf16(tmem + st * kNC, ad, bd, idesc_s, (a | kk) ? 1u : 0u);
             }
@@ -299,15 +369,16 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* xrow = xs + h * kNC;
-    const uint32_t xrow_peer = mapa(smem_u32(xrow), peer);
+    const uint32_t xs_peer = mapa(smem_u32(xs), peer);  // our partial goes there
     const uint32_t x_full_peer = mapa(smem_u32(x_full), peer);
     const uint32_t x_empty_peer = mapa(smem_u32(x_empty), peer);
     uint8_t* prow = ps + h * 128;
+    uint8_t* stage = ps + quarter * 4096;  // output staging (P is idle between units)
     int gc = 0;
     bool stop = false;
     for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
-      if (!mbar_wait(meta_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(meta_full, ui & 1, abort_flag, p.status,
+                                             DSA_FLAG_TIMEOUT))) break;
       const int nv = *meta_nv;
       __syncwarp();
       if (lane == 0) mbar_arrive(meta_empty);
@@ -318,9 +389,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
       for (int c = 0; c < nch; ++c, ++gc) {
         const int sb = gc & 1;
         const int rows_in = min(kNC, n - c * kNC);
-        if (!mbar_wait(&s_full[sb], (gc >> 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
-          stop = true; break;
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gc >> 1) & 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) { stop = true; break; }
         tc_fence_after();
         float s[kNC];
         {
@@ -335,23 +405,29 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[sb]);
-        // exchange the partial logits with the peer CTA
-        if (!mbar_wait_cluster(x_empty, (gc & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+        // exchange the partial logits: push ours into the peer's buffer ([16][128]
+        // float4, so a warp's stores are contiguous), read the peer's from our own
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_empty, (gc & 1) ^ 1, abort_flag,
+                                                       p.status, DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
 #pragma unroll
         for (int q = 0; q < kNC / 4; ++q)
-          reinterpret_cast<float4*>(xrow)[q ^ (h & 15)] =
-              make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
+          st_cluster_f4(xs_peer + (uint32_t)((q * kH + h) * 16),
+                        make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
         mbar_arrive_remote(x_full_peer);
-        if (!mbar_wait_cluster(x_full, gc & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_full, gc & 1, abort_flag, p.status,
+                                                       DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
+        float4 xo[kNC / 4];
+#pragma unroll
+        for (int q = 0; q < kNC / 4; ++q) xo[q] = xs[q * kH + h];
+        mbar_arrive_remote(x_empty_peer);
         float m_c = -INFINITY;
 #pragma unroll
         for (int q = 0; q < kNC / 4; ++q) {
-          const float4 o = ld_cluster_f4(xrow_peer + (uint32_t)((q ^ (h & 15)) * 16));
-          const float other[4] = {o.x, o.y, o.z, o.w};
+          const float other[4] = {xo[q].x, xo[q].y, xo[q].z, xo[q].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * q + e;
@@ -362,16 +438,14 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             m_c = fmaxf(m_c, s[i]);
           }
         }
-        mbar_arrive_remote(x_empty_peer);
         // running max: move the reference only when it grows by more than 2^8
         const bool grow = m_c > m_ref + kRescaleLog2;
         const float m_new = grow ? m_c : m_ref;
-        const float factor = grow ? exp2f(m_ref - m_new) : 1.f;
+        const float factor = grow ? ex2(m_ref - m_new) : 1.f;
         l *= factor;
         if (__any_sync(0xffffffffu, grow && c > 0)) {
-          if (!mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
-            stop = true; break;
-          }
+          if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status,
+                                                 DSA_FLAG_TIMEOUT))) { stop = true; break; }
           tc_fence_after();
           for (int b = 0; b < 8; ++b) {
             uint32_t r[32];
@@ -386,15 +460,14 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
         uint32_t pk[kNC / 2];
 #pragma unroll
         for (int i = 0; i < kNC / 2; ++i) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(s[2 * i] - m_ref),
-                                                          exp2f(s[2 * i + 1] - m_ref));
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(s[2 * i] - m_ref),
+                                                          ex2(s[2 * i + 1] - m_ref));
           const float2 f2 = __bfloat1622float2(b2);
           l += f2.x + f2.y;
           pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        if (!mbar_wait(p_empty, (gc & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
-          stop = true; break;
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait(p_empty, (gc & 1) ^ 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) { stop = true; break; }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           *reinterpret_cast<uint4*>(prow + ((j ^ (h & 7)) * 16)) =
@@ -408,47 +481,30 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
       // ---- epilogue of the unit ----
       const bool have = nch > 0;
       if (have) {
-        if (!mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) break;
         tc_fence_after();
       }
+      const int64_t row0 = (int64_t)t * kH + quarter * 32;  // first head row of this warp
       if (p.nsplit == 1) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int64_t obase = ((int64_t)t * kH + h) * kDC + colbase;
         for (int b = 0; b < 8; ++b) {
           uint32_t r[32];
           if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
           else
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
-          if (p.out_f32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + 32 * b);
+          float o[32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                 __uint_as_float(r[4 * i + 2]) * inv,
-                                 __uint_as_float(r[4 * i + 3]) * inv);
-          } else {
-            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + 32 * b);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t w4[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 b2 =
-                    __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
-                                          __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
-                w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
-              }
-              o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-          }
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv;
+          store_block(o, p.out_f32, p.out, row0, colbase + 32 * b, stage, lane);
         }
         if (rank == 0 && p.lse)
           p.lse[(int64_t)t * kH + h] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
       } else {
-        // split of a row: publish (O, m, l); the last split of the row merges them
+        // split of a row: publish (O, m, l); the second split of the row to finish merges
         const int64_t slot = ((int64_t)t * p.nsplit + sp) * 2 + rank;
-        float* po = p.part_o + (slot * kH + h) * 256;
+        float4* po = p.part_o + slot * (64 * kH);
         for (int b = 0; b < 8; ++b) {
           uint32_t r[32];
           if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
@@ -457,71 +513,59 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             for (int i = 0; i < 32; ++i) r[i] = 0u;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(po + 32 * b)[i] =
+            po[(8 * b + i) * kH + h] =
                 make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
         }
         p.part_ml[(slot * kH + h) * 2] = m_ref;
         p.part_ml[(slot * kH + h) * 2 + 1] = l;
+        // all 128 partial rows are out before the arrival count moves (bounded waits)
         __threadfence();
-        named_bar(1, 128);
-        if (threadIdx.x == 64) *s_last = atomicAdd(p.counters + t * 2 + rank, 1) == p.nsplit - 1;
-        named_bar(1, 128);
+        mbar_arrive(sync_a);
+        if (threadIdx.x == 64) {
+          const bool okw = mbar_wait(sync_a, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT);
+          *s_last = okw && atomicAdd(p.counters + t * 2 + rank, 1) == p.nsplit - 1;
+          mbar_arrive(sync_b);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(sync_b, ui & 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) break;
         if (*s_last) {
           // The other split's (O, m, l) of this column half: one bulk copy of its
-          // 128 KB into the (now idle) query/KV area, then each thread merges its head row.
+          // 128 KB into the (now idle) query/KV area, then each thread merges its head.
           __threadfence();
           const int64_t other = ((int64_t)t * p.nsplit + (1 - sp)) * 2 + rank;
-          float* po2 = reinterpret_cast<float*>(qs);
+          float4* po2 = reinterpret_cast<float4*>(qs);
           if (threadIdx.x == 64) {
             fence_proxy_async_all();
             mbar_arrive_expect_tx(drain + 1, kH * 256 * 4);
             for (int c = 0; c < 8; ++c)
-              bulk_load(po2 + c * 4096, p.part_o + (other * kH) * 256 + c * 4096, 16384, drain + 1);
+              bulk_load(po2 + c * 1024, p.part_o + other * (64 * kH) + c * 1024, 16384, drain + 1);
           }
           const float mo = __ldcg(p.part_ml + (other * kH + h) * 2);
           const float lo2 = __ldcg(p.part_ml + (other * kH + h) * 2 + 1);
           const float M = fmaxf(m_ref, mo);
-          const float wa = l > 0.f ? exp2f(m_ref - M) : 0.f;
-          const float wb = lo2 > 0.f ? exp2f(mo - M) : 0.f;
+          const float wa = l > 0.f ? ex2(m_ref - M) : 0.f;
+          const float wb = lo2 > 0.f ? ex2(mo - M) : 0.f;
           const float wsum = wa * l + wb * lo2;
           const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-          if (!mbar_wait(drain + 1, 0, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
-          const float* orow = po2 + h * 256;
-          const int64_t obase = ((int64_t)t * kH + h) * kDC + colbase;
+          if (!__all_sync(0xffffffffu, mbar_wait(drain + 1, 0, abort_flag, p.status,
+                                                 DSA_FLAG_TIMEOUT))) break;
           for (int b = 0; b < 8; ++b) {
             uint32_t r[32];
             if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
             else
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = 0u;
-            float res[32];
+            float o[32];
 #pragma unroll
-            for (int qq = 0; qq < 8; ++qq) {
-              const float4 o = reinterpret_cast<const float4*>(orow + 32 * b)[qq];
-              res[4 * qq] = (wa * __uint_as_float(r[4 * qq]) + wb * o.x) * inv;
-              res[4 * qq + 1] = (wa * __uint_as_float(r[4 * qq + 1]) + wb * o.y) * inv;
-              res[4 * qq + 2] = (wa * __uint_as_float(r[4 * qq + 2]) + wb * o.z) * inv;
-              res[4 * qq + 3] = (wa * __uint_as_float(r[4 * qq + 3]) + wb * o.w) * inv;
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = po2[(8 * b + i) * kH + h];
+              o[4 * i] = (wa * __uint_as_float(r[4 * i]) + wb * x.x) * inv;
+              o[4 * i + 1] = (wa * __uint_as_float(r[4 * i + 1]) + wb * x.y) * inv;
+              o[4 * i + 2] = (wa * __uint_as_float(r[4 * i + 2]) + wb * x.z) * inv;
+              o[4 * i + 3] = (wa * __uint_as_float(r[4 * i + 3]) + wb * x.w) * inv;
             }
-            if (p.out_f32) {
-              float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + 32 * b);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                o[i] = make_float4(res[4 * i], res[4 * i + 1], res[4 * i + 2], res[4 * i + 3]);
-            } else {
-              uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + 32 * b);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(res[8 * i + 2 * e], res[8 * i + 2 * e + 1]);
-                  w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
-                }
-                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-              }
-            }
+            store_block(o, p.out_f32, p.out, row0, colbase + 32 * b, stage, lane);
           }
           if (rank == 0 && p.lse)
             p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f
@@ -546,10 +590,8 @@ bool sfa_tc_eligible(const SfaArgs& a) {
          a.top_k <= kMaxTopK;
 }
 
-int sfa_tc_nsplit(int total_q) {
-  if (total_q <= 0) return 1;
-  return num_sms() >= 4 * total_q ? 2 : 1;
-}
+// Split each row over 2 clusters when that still leaves every cluster one unit.
+int sfa_tc_nsplit(int total_q) { return total_q > 0 && num_sms() >= 4 * total_q ? 2 : 1; }
 
 size_t sfa_tc_scratch_bytes(int total_q) {
   const int ns = sfa_tc_nsplit(total_q);
@@ -562,12 +604,9 @@ size_t sfa_tc_scratch_bytes(int total_q) {
 int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
   const int ns = sfa_tc_nsplit(a.seqs.total_q);
-  CUtensorMap qmap, kvmap;
+  CUtensorMap qmap;
   int rc = make_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD,
                         (uint64_t)a.seqs.total_q * kH, kD * 2, 64, kH);
-  if (rc != DSA_OK) return rc;
-  rc = make_tmap_2d(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kD, (uint64_t)a.seqs.total_k,
-                    kD * 2, 64, 1);
   if (rc != DSA_OK) return rc;
   Params p{};
   p.seqs = a.seqs;
@@ -576,13 +615,14 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   p.nsplit = ns;
   p.out_f32 = a.out_dtype == DSA_F32;
   p.idx = a.idx;
+  p.kv = static_cast<const __nv_bfloat16*>(a.kv);
   p.out = a.out;
   p.lse = a.lse;
   p.status = a.status;
   if (ns > 1) {
     const size_t slots = (size_t)a.seqs.total_q * ns * 2;
     char* b = static_cast<char*>(scratch);
-    p.part_o = reinterpret_cast<float*>(b);
+    p.part_o = reinterpret_cast<float4*>(b);
     b += align_up(slots * kH * 256 * 4, 256);
     p.part_ml = reinterpret_cast<float*>(b);
     b += align_up(slots * kH * 2 * 4, 256);
@@ -596,7 +636,7 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   const int64_t units = (int64_t)a.seqs.total_q * ns;
   const int max_clusters = num_sms() / 2;
   const int clusters = (int)(units < max_clusters ? units : max_clusters);
-  DSA_LAUNCH("sfa_tc", stream, sfa_tc_kernel<<<2 * clusters, 192, kSmem, stream>>>(qmap, kvmap, p));
+  DSA_LAUNCH("sfa_tc", stream, sfa_tc_kernel<<<2 * clusters, 192, kSmem, stream>>>(qmap, p));
   return check_launch("sfa_tc");
 }
 
