@@ -190,7 +190,6 @@ size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 
 // starts of the tensor-core schedule.  The fused forward adds the indices.
 struct IndexerScratch {
   float* scores;
-  int32_t* tile_start;
   int32_t* idx;
   void* sfa;
 };
@@ -204,13 +203,11 @@ size_t sfa_scratch_bytes(const dsa_problem* p) {
 size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
   const size_t o_scores = c.take(scores_bytes(p));
-  const size_t o_tiles = c.take(indexer_tc_tile_start_bytes(p->total_q));
   const size_t o_idx = c.take(idx_bytes(p));
   const size_t o_sfa = c.take(sfa_scratch_bytes(p));
   if (out) {
     char* b = static_cast<char*>(ws);
     out->scores = reinterpret_cast<float*>(b + o_scores);
-    out->tile_start = reinterpret_cast<int32_t*>(b + o_tiles);
     out->idx = reinterpret_cast<int32_t*>(b + o_idx);
     out->sfa = b + o_sfa;
   }
@@ -224,11 +221,7 @@ size_t ws_sfa(const dsa_problem* p) {
   c.take(sfa_scratch_bytes(p));
   return c.off;
 }
-size_t ws_indexer_scores(const dsa_problem* p) {
-  Carve c;
-  c.take(indexer_tc_tile_start_bytes(p->total_q));
-  return c.off;
-}
+size_t ws_indexer_scores(const dsa_problem*) { return kStatusBytes; }
 
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (!ws) return set_error(DSA_ERR_WORKSPACE, "workspace is NULL");
@@ -278,7 +271,7 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
   const int64_t ld = scores_ld(p);
   if (indexer_tc_eligible(ia))
-    DSA_TRY(launch_indexer_tc(ia, sc.scores, ld, sc.tile_start, s));
+    DSA_TRY(launch_indexer_tc(ia, sc.scores, ld, s));
   else
     DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, ld, s));
   TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws)};
@@ -352,10 +345,7 @@ int dsa_indexer_scores(const dsa_problem* p, const void* q_idx, const void* k_id
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (indexer_tc_eligible(ia)) {
-    Carve c;
-    int32_t* tiles = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
-                                                c.take(indexer_tc_tile_start_bytes(p->total_q)));
-    DSA_TRY(launch_indexer_tc(ia, scores, ld, tiles, s));
+    DSA_TRY(launch_indexer_tc(ia, scores, ld, s));
     return launch_mask_tail(seqs_of(p), scores, ld, static_cast<uint32_t*>(ws), s);
   }
   return launch_indexer_scores_simt(ia, scores, ld, s);

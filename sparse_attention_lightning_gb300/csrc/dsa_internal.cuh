@@ -117,9 +117,7 @@ int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
 
 // tcgen05 indexer (H_I = 64, d_I = 128, bf16 or FP8): writes scores[t, s] for s <= pos(t).
 bool indexer_tc_eligible(const IndexerArgs& a);
-size_t indexer_tc_tile_start_bytes(int total_q);
-int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, int32_t* tile_start,
-                      cudaStream_t stream);
+int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream);
 
 // Fill scores[t, s] = -inf for pos(t) < s < ld.
 int launch_mask_tail(const Seqs& seqs, float* scores, int64_t ld, uint32_t* status,

@@ -14,12 +14,16 @@
 // without any cross-thread reduction.  For FP8 the scales fold in as
 // I = k_scale[s] · Σ_j (w·q_scale)[t,j] · ReLU(z8) (all scales are positive).
 //
-// Schedule: the tiles of all rows are laid end to end; each persistent CTA
-// takes one contiguous, equal share, so a long-history row is simply spread
-// over more CTAs than a short one.  Warp roles: warp 0 issues TMA loads
-// (a 4-8 stage ring of key tiles, a 2-slot ring of query blocks), warp 1 owns
-// TMEM and issues the MMAs, warps 2..5 run the epilogue on a double-buffered
-// TMEM accumulator.  Every wait is bounded (DSA_FLAG_TIMEOUT).
+// Schedule: the tiles of all rows are laid end to end (a causal row at
+// position p has floor(p/128) + 1 of them) and each persistent CTA takes one
+// contiguous, equal share, so a long-history row is simply spread over more
+// CTAs than a short one.  Each CTA derives the tile layout itself from cu_q /
+// cu_k: per sequence the tile count is F(L) - F(L - T) with
+// F(n) = Σ_{p<n} (floor(p/128) + 1) = n + 64 q (q - 1) + r q  (q = n / 128, r = n % 128).
+// Warp roles: warp 0 issues TMA loads (a 4-8 stage ring of key tiles, a 2-slot
+// ring of query blocks), warp 1 owns TMEM and issues the MMAs, warps 2..5 run
+// the epilogue on a double-buffered TMEM accumulator.  Every wait is bounded
+// (DSA_FLAG_TIMEOUT).
 #include "dsa_internal.cuh"
 #include "tc_sm100.cuh"
 
@@ -27,6 +31,8 @@ namespace dsa {
 namespace {
 
 using namespace tc;
+
+constexpr int kMaxSeqs = 4096;  // sequences per launch on this path (tile table in smem)
 
 template <bool FP8>
 struct Cfg {
@@ -42,7 +48,7 @@ struct Cfg {
   static constexpr int KSTEPS = FP8 ? 4 : 8;       // MMAs per tile (32 B of K each)
   static constexpr int ACC_COLS = HI;              // fp32 accumulator columns
   static constexpr int TMEM_COLS = 2 * ACC_COLS;   // double buffered
-  static constexpr int SMEM = NS * KTILE + 2 * QTILE + 2048 /*bars etc*/ + 1024 /*align*/;
+  static constexpr int SMEM_FIXED = NS * KTILE + 2 * QTILE + 2048 /*bars etc*/ + 1024 /*align*/;
 };
 
 struct Params {
@@ -52,31 +58,84 @@ struct Params {
   const float* k_scale;
   float* scores;
   int64_t ld;
-  const int32_t* tile_start;  // [total_q + 1]: first tile of each row, then the total
   uint32_t* status;
 };
 
-// Row info without flagging (the tile-count pass has flagged bad rows already).
-__device__ __forceinline__ void row_of(const Seqs& s, int t, int& pos, int& k0) {
-  int lo = 0, hi = s.B - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(s.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  const int q1 = __ldg(s.cu_q + lo + 1);
-  k0 = __ldg(s.cu_k + lo);
-  const int L = __ldg(s.cu_k + lo + 1) - k0;
-  pos = L - (q1 - t);
+__device__ __forceinline__ int64_t ftiles(int64_t n) {  // Σ_{p<n} (floor(p/128) + 1)
+  const int64_t q = n >> 7, r = n & 127;
+  return n + 64 * q * (q - 1) + r * q;
 }
 
-// First row whose tile range contains g (tile_start is non-decreasing).
-__device__ __forceinline__ int row_of_tile(const int32_t* ts, int nrows, int g) {
-  int lo = 0, hi = nrows - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(ts + mid) <= g) lo = mid; else hi = mid - 1;
+// Per-sequence tile table built in shared memory by every CTA.
+struct SeqTab {
+  const int32_t* st;  // [B+1] first tile of each sequence, then the total
+  const int32_t* cq;  // [B+1] cu_q
+  const int32_t* ck;  // [B+1] cu_k
+  int B;
+};
+
+// Walks the CTA's items (row tile by row tile) in order; all roles run one.
+struct Cursor {
+  int b, i, T, L, q0, k0;  // sequence, query index in it, its sizes and offsets
+  int t, pos, j, ntiles;   // packed row, its position, current tile, tiles of the row
+
+  __device__ __forceinline__ void load_seq(const SeqTab& s) {
+    q0 = s.cq[b]; T = s.cq[b + 1] - q0;
+    k0 = s.ck[b]; L = s.ck[b + 1] - k0;
   }
-  return lo;
+  __device__ __forceinline__ void set_row() {
+    t = q0 + i;
+    pos = L - T + i;
+    ntiles = pos / 128 + 1;
+  }
+  __device__ __forceinline__ void locate(const SeqTab& s, int g) {
+    int lo = 0, hi = s.B - 1;  // last b with st[b] <= g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s.st[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    load_seq(s);
+    const int64_t gl = g - s.st[b], base = ftiles(L - T);
+    int ilo = 0, ihi = T - 1;  // last i with F(L - T + i) - base <= gl
+    while (ilo < ihi) {
+      const int mid = (ilo + ihi + 1) >> 1;
+      if (ftiles(L - T + mid) - base <= gl) ilo = mid; else ihi = mid - 1;
+    }
+    i = ilo;
+    set_row();
+    j = (int)(gl - (ftiles(L - T + i) - base));
+  }
+  __device__ __forceinline__ void advance(const SeqTab& s) {
+    if (++j < ntiles) return;
+    j = 0;
+    if (++i == T) {
+      i = 0;
+      do { ++b; } while (b < s.B - 1 && s.st[b + 1] == s.st[b]);  // skip tile-less sequences
+      load_seq(s);
+    }
+    set_row();
+  }
+};
+
+__device__ __forceinline__ uint32_t scan192(uint32_t v, uint32_t* ws, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+  for (int w = 0; w < 6; ++w) {
+    if (w < warp) before += ws[w];
+    tot += ws[w];
+  }
+  *total = tot;
+  __syncthreads();
+  return before + x - v;
 }
 
 template <bool FP8>
@@ -99,10 +158,44 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   float* wsm = reinterpret_cast<float*>(drain + 2);  // [4 epilogue warps][64]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsm + 4 * 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* scan_ws = tmem_slot + 2;                   // [6]
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + C::SMEM_FIXED - 1024);
+  const int B = p.seqs.B;
+  int32_t* st = tab;
+  int32_t* cq = st + (B + 1);
+  int32_t* ck = cq + (B + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nrows = p.seqs.total_q;
-  const int total = __ldg(p.tile_start + nrows);
+
+  // ---- tile table of the sequences (every CTA builds its own copy) ----
+  uint32_t carry = 0;
+  for (int base = 0; base < B; base += 192) {
+    const int b = base + threadIdx.x;
+    uint32_t n = 0;
+    if (b < B) {
+      const int q0 = __ldg(p.seqs.cu_q + b), q1 = __ldg(p.seqs.cu_q + b + 1);
+      const int k0 = __ldg(p.seqs.cu_k + b), k1 = __ldg(p.seqs.cu_k + b + 1);
+      const int T = q1 - q0, L = k1 - k0;
+      const bool ok = q0 >= 0 && T >= 0 && T <= L && k0 >= 0 && k1 <= p.seqs.total_k &&
+                      L <= p.seqs.max_k_len && q1 <= p.seqs.total_q;
+      if (ok) n = (uint32_t)(ftiles(L) - ftiles(L - T));
+      else if (blockIdx.x == 0) atomicOr(p.status, DSA_FLAG_BAD_SEQS);
+      cq[b] = q0;
+      ck[b] = k0;
+    }
+    uint32_t tot;
+    const uint32_t excl = scan192(n, scan_ws, &tot);
+    if (b < B) st[b] = (int32_t)(carry + excl);
+    carry += tot;
+  }
+  if (threadIdx.x == 0) {
+    st[B] = (int32_t)carry;
+    cq[B] = __ldg(p.seqs.cu_q + B);
+    ck[B] = __ldg(p.seqs.cu_k + B);
+  }
+  __syncthreads();
+  const SeqTab tabs{st, cq, ck, B};
+  const int total = st[B];
   const int g0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int g1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   if (g0 >= g1) return;
@@ -129,30 +222,28 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      int t = row_of_tile(p.tile_start, nrows, g0), cur = -1, rows_seen = 0, pos = 0, k0 = 0;
-      int issued = 0;
+      Cursor cur;
+      cur.locate(tabs, g0);
+      int rows_seen = 0, issued = 0;
       for (int g = g0, it = 0; g < g1; ++g, ++it) {
-        while (__ldg(p.tile_start + t + 1) <= g) ++t;
-        if (t != cur) {
-          cur = t;
-          row_of(p.seqs, t, pos, k0);
+        if (g > g0) cur.advance(tabs);
+        if (g == g0 || cur.j == 0) {
           const int slot = rows_seen & 1;
           if (!mbar_wait(&q_empty[slot], ((rows_seen >> 1) & 1) ^ 1, abort_flag, p.status,
                          DSA_FLAG_TIMEOUT)) break;
           mbar_arrive_expect_tx(&q_full[slot], C::QTILE);
           for (int a = 0; a < C::ATOMS; ++a)
             tma_load_2d(qs + slot * C::QTILE + a * (C::HI * 128), &qmap, &q_full[slot],
-                        a * (128 / C::ES), t * C::HI);
+                        a * (128 / C::ES), cur.t * C::HI);
           ++rows_seen;
         }
-        const int j = g - __ldg(p.tile_start + t);
         const int s = it % C::NS;
         if (!mbar_wait(&k_empty[s], ((it / C::NS) & 1) ^ 1, abort_flag, p.status,
                        DSA_FLAG_TIMEOUT)) break;
         mbar_arrive_expect_tx(&k_full[s], C::KTILE);
         for (int a = 0; a < C::ATOMS; ++a)
           tma_load_2d_hint(ks + s * C::KTILE + a * (C::BM * 128), &kmap, &k_full[s],
-                           a * (128 / C::ES), k0 + j * C::BM, pol);
+                           a * (128 / C::ES), cur.k0 + cur.j * C::BM, pol);
         issued = it + 1;
       }
       // every key-tile copy issued has landed before the CTA may exit
@@ -165,11 +256,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = FP8 ? idesc_e4m3(128, C::HI) : idesc_bf16(128, C::HI);
-      int t = row_of_tile(p.tile_start, nrows, g0), cur = -1, rows_seen = 0;
+      Cursor cur;
+      cur.locate(tabs, g0);
+      int rows_seen = 0;
       for (int g = g0, it = 0; g < g1; ++g, ++it) {
-        while (__ldg(p.tile_start + t + 1) <= g) ++t;
-        if (t != cur) {
-          cur = t;
+        if (g > g0) cur.advance(tabs);
+        if (g == g0 || cur.j == 0) {
           if (!mbar_wait(&q_full[rows_seen & 1], (rows_seen >> 1) & 1, abort_flag, p.status,
                          DSA_FLAG_TIMEOUT)) break;
           tc_fence_after();
@@ -193,8 +285,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         mma_commit(&k_empty[s]);
         mma_commit(&acc_full[acc]);
-        const bool last_of_row = (g + 1 == g1) || (__ldg(p.tile_start + t + 1) == g + 1);
-        if (last_of_row) mma_commit(&q_empty[slot]);
+        if (g + 1 == g1 || cur.j + 1 == cur.ntiles) mma_commit(&q_empty[slot]);
       }
       // every MMA issued has completed before TMEM is released
       mma_commit(drain);
@@ -204,25 +295,25 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // ---------------- epilogue: warps 2..5, TMEM lane quarter warp % 4 ----------------
     const int quarter = warp & 3;
     float* wq = wsm + (warp - 2) * 64;
-    int t = row_of_tile(p.tile_start, nrows, g0), cur = -1, pos = 0, k0 = 0;
+    Cursor cur;
+    cur.locate(tabs, g0);
     for (int g = g0, it = 0; g < g1; ++g, ++it) {
-      while (__ldg(p.tile_start + t + 1) <= g) ++t;
-      if (t != cur) {
-        cur = t;
-        row_of(p.seqs, t, pos, k0);
+      if (g > g0) cur.advance(tabs);
+      if (g == g0 || cur.j == 0) {
         __syncwarp();
-        float w0 = __ldg(p.w + (int64_t)t * C::HI + lane);
-        float w1 = __ldg(p.w + (int64_t)t * C::HI + lane + 32);
+        float w0 = __ldg(p.w + (int64_t)cur.t * C::HI + lane);
+        float w1 = __ldg(p.w + (int64_t)cur.t * C::HI + lane + 32);
         if (FP8) {
-          w0 *= __ldg(p.q_scale + (int64_t)t * C::HI + lane);
-          w1 *= __ldg(p.q_scale + (int64_t)t * C::HI + lane + 32);
+          w0 *= __ldg(p.q_scale + (int64_t)cur.t * C::HI + lane);
+          w1 *= __ldg(p.q_scale + (int64_t)cur.t * C::HI + lane + 32);
         }
         wq[lane] = w0;
         wq[lane + 32] = w1;
         __syncwarp();
       }
       const int acc = it & 1;
-      if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT))
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it >> 1) & 1, abort_flag, p.status,
+                                             DSA_FLAG_TIMEOUT)))
         break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS;
@@ -238,11 +329,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      const int j = g - __ldg(p.tile_start + t);
-      const int s = j * C::BM + quarter * 32 + lane;
-      if (s <= pos) {
-        if (FP8) sum *= __ldg(p.k_scale + k0 + s);
-        p.scores[(int64_t)t * p.ld + s] = sum;
+      const int s = cur.j * C::BM + quarter * 32 + lane;
+      if (s <= cur.pos) {
+        if (FP8) sum *= __ldg(p.k_scale + cur.k0 + s);
+        p.scores[(int64_t)cur.t * p.ld + s] = sum;
       }
     }
   }
@@ -255,46 +345,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
 }
 
-// Tiles per row (ceil((pos+1)/128)) and their running start; 0 for invalid rows.
-__global__ void __launch_bounds__(1024) row_tiles_kernel(Seqs seqs, int32_t* tile_start,
-                                                          uint32_t* status) {
-  __shared__ uint32_t warp_sums[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t carry = 0;
-  for (int base = 0; base < seqs.total_q; base += 1024) {
-    const int t = base + tid;
-    uint32_t n = 0;
-    RowInfo r;
-    if (t < seqs.total_q && query_row_info(seqs, t, r, status)) n = (uint32_t)(r.pos / 128 + 1);
-    uint32_t x = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t s = warp_sums[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += y;
-      }
-      warp_sums[lane] = s;
-    }
-    __syncthreads();
-    const uint32_t excl = carry + (warp ? warp_sums[warp - 1] : 0u) + x - n;
-    if (t < seqs.total_q) tile_start[t] = (int32_t)excl;
-    carry += warp_sums[31];
-    __syncthreads();
-  }
-  if (tid == 0) tile_start[seqs.total_q] = (int32_t)carry;
-}
-
 template <bool FP8>
-int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, int32_t* tile_start,
-                 cudaStream_t stream) {
+int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
   using C = Cfg<FP8>;
   CUtensorMap kmap, qmap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -304,36 +356,31 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, int32_t* tile_
   rc = make_tmap_2d(&qmap, dt, a.q_idx, C::DI, (uint64_t)a.seqs.total_q * C::HI, C::ROWB,
                     128 / C::ES, C::HI);
   if (rc != DSA_OK) return rc;
+  const int smem = C::SMEM_FIXED + (int)align_up(3 * sizeof(int32_t) * (a.seqs.B + 1), 16);
   auto kern = indexer_tc_kernel<FP8>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("indexer_tc: smem attribute");
-  DSA_LAUNCH("row_tiles", stream,
-             row_tiles_kernel<<<1, 1024, 0, stream>>>(a.seqs, tile_start, a.status));
-  rc = check_launch("row_tiles");
-  if (rc != DSA_OK) return rc;
   const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + C::BM - 1) / C::BM);
   const int grid = (int)(bound < num_sms() ? bound : num_sms());
-  Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, tile_start, a.status};
+  Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status};
   DSA_LAUNCH(FP8 ? "indexer_tc_fp8" : "indexer_tc_bf16", stream,
-             kern<<<grid, 192, C::SMEM, stream>>>(kmap, qmap, p));
+             kern<<<grid, 192, smem, stream>>>(kmap, qmap, p));
   return check_launch("indexer_tc");
 }
 
 }  // namespace
 
 bool indexer_tc_eligible(const IndexerArgs& a) {
+  // tiles of the whole problem must stay below 2^31 (int32 item indices)
+  const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + 127) / 128);
   return (a.idx_dtype == DSA_BF16 || a.idx_dtype == DSA_FP8_E4M3) && a.h_idx == 64 &&
-         a.d_idx == 128;
+         a.d_idx == 128 && a.seqs.B <= kMaxSeqs && bound < (int64_t(1) << 31);
 }
 
-size_t indexer_tc_tile_start_bytes(int total_q) { return sizeof(int32_t) * ((size_t)total_q + 1); }
-
-int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, int32_t* tile_start,
-                      cudaStream_t stream) {
+int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
-  if (a.idx_dtype == DSA_FP8_E4M3) return launch_typed<true>(a, scores, ld, tile_start, stream);
-  return launch_typed<false>(a, scores, ld, tile_start, stream);
+  if (a.idx_dtype == DSA_FP8_E4M3) return launch_typed<true>(a, scores, ld, stream);
+  return launch_typed<false>(a, scores, ld, stream);
 }
 
 }  // namespace dsa

@@ -30,8 +30,9 @@
 //    once P is ready, O += P · V (M=128, N=256, K=64, V read MN-major straight
 //    from the gathered tile);
 //  * softmax warps (one thread per head): read S from TMEM, push their partial
-//    into the peer CTA's shared memory (coalesced remote stores), read the
-//    peer's from their own, keep a running max (O is rescaled only when the max
+//    into the peer CTA's shared memory with st.async (coalesced asynchronous
+//    remote stores that complete on the peer's mbarrier), read the peer's from
+//    their own, keep a running max (O is rescaled only when the max
 //    grows by more than 2^8), write P = 2^(x - m) as bf16 for the PV MMA.
 //
 // Decode rows are split over 2 clusters when there are few queries; the second
@@ -167,8 +168,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
   uint64_t* p_full = bars + 10;
   uint64_t* p_empty = bars + 11;
   uint64_t* pv_done = bars + 12;
-  uint64_t* x_full = bars + 13;      // peer's 128 softmax threads arrive here
-  uint64_t* x_empty = bars + 14;
+  uint64_t* x_full = bars + 13;      // the peer's st.async bytes land here (32 KB per chunk)
+  uint64_t* x_empty = bars + 14;     // the peer's 4 softmax warps: buffer read
   uint64_t* meta_full = bars + 15;
   uint64_t* meta_empty = bars + 16;
   uint64_t* drain = bars + 17;       // [2]: MMA drain, merge copy
@@ -194,7 +195,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
     }
     mbar_init(q_full, 1); mbar_init(q_empty, 1);
     mbar_init(p_full, 4); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
-    mbar_init(x_full, 128); mbar_init(x_empty, 128);
+    mbar_init(x_full, 1); mbar_init(x_empty, 4);
     mbar_init(meta_full, 1); mbar_init(meta_empty, 5);
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
@@ -405,17 +406,18 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[sb]);
-        // exchange the partial logits: push ours into the peer's buffer ([16][128]
-        // float4, so a warp's stores are contiguous), read the peer's from our own
+        // exchange the partial logits: st.async ours into the peer's buffer ([16][128]
+        // float4, so a warp's stores are contiguous; the bytes complete on the peer's
+        // x_full), then read the peer's from our own buffer
+        if (threadIdx.x == 64) mbar_arrive_expect_tx(x_full, kXBytes);
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_empty, (gc & 1) ^ 1, abort_flag,
                                                        p.status, DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
 #pragma unroll
         for (int q = 0; q < kNC / 4; ++q)
-          st_cluster_f4(xs_peer + (uint32_t)((q * kH + h) * 16),
-                        make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
-        mbar_arrive_remote(x_full_peer);
+          st_async_f4(xs_peer + (uint32_t)((q * kH + h) * 16),
+                      make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]), x_full_peer);
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_full, gc & 1, abort_flag, p.status,
                                                        DSA_FLAG_TIMEOUT))) {
           stop = true; break;
@@ -423,7 +425,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
         float4 xo[kNC / 4];
 #pragma unroll
         for (int q = 0; q < kNC / 4; ++q) xo[q] = xs[q * kH + h];
-        mbar_arrive_remote(x_empty_peer);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(x_empty_peer);  // our buffer may be refilled
         float m_c = -INFINITY;
 #pragma unroll
         for (int q = 0; q < kNC / 4; ++q) {

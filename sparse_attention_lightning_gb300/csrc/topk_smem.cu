@@ -5,6 +5,7 @@
 // Performance Optimization for New-Architecture LLMs", §4.1), with the same
 // contract as topk_rows.cu: the n = min(top_k, pos+1) largest scores, ties to
 // the smaller position, written in ascending position order, -1 padded.
+// 1024 threads per row; every pass over the keys is warp-coalesced.
 //
 // The row is read once from global memory into shared memory as
 // order-preserving uint32 keys, with its min and max.  The radix select runs on
@@ -20,34 +21,11 @@
 namespace dsa {
 namespace {
 
-constexpr int kT = 512;
+constexpr int kT = 1024;
 constexpr int kW = kT / 32;
 constexpr int kMaxKeys = 40960;
 constexpr int kCandCap = 4096;
 constexpr size_t kSmem = sizeof(uint32_t) * ((size_t)kMaxKeys + kW * 256 + 256 + kCandCap);
-
-__device__ __forceinline__ uint32_t scan_excl(uint32_t v, uint32_t* warp_sums) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t s = lane < kW ? warp_sums[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < kW) warp_sums[lane] = s;
-  }
-  __syncthreads();
-  return (warp ? warp_sums[warp - 1] : 0u) + x - v;
-}
 
 __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   extern __shared__ uint32_t sm[];
@@ -55,7 +33,7 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   uint32_t* hist = keys + kMaxKeys;     // [kW][256]
   uint32_t* tot = hist + kW * 256;      // [256]
   uint32_t* cand = tot + 256;           // [kCandCap]
-  __shared__ uint32_t red_min[kW], red_max[kW], warp_sums[kW];
+  __shared__ uint32_t red_min[kW], red_max[kW];
   __shared__ uint32_t s_digit, s_above, s_cnt, s_ncand;
 
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -199,53 +177,39 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   const uint32_t T = kmin + prefix;  // the n-th largest key; `need` of the keys equal to it are kept
 
   // --- ordered write -------------------------------------------------------------------
-  const int m = (n + 32 * kT - 1) / (32 * kT);  // 32-key chunks per thread
-  const int base = tid * 32 * m;
+  // Warp w owns the contiguous key range [w*seg, (w+1)*seg).  Pass A counts its keys
+  // above / equal to T with ballots; a scan over the 16 warp totals gives each warp
+  // its offsets; pass B places every selected key (ballot ranks within the warp).
+  const int seg = ((n + kW - 1) / kW + 31) / 32 * 32;
+  const int w0 = warp * seg, w1 = min(n, w0 + seg);
+  const unsigned lt = (1u << lane) - 1u;
   uint32_t cg = 0, ce = 0;
-  for (int c = 0; c < m; ++c) {
-#pragma unroll 8
-    for (int jj = 0; jj < 32; ++jj) {
-      const int i = base + c * 32 + ((jj + lane) & 31);
-      if (i < n) {
-        const uint32_t key = keys[i];
-        cg += key > T;
-        ce += key == T;
-      }
-    }
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    cg += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
+    ce += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
   }
-  const uint32_t pre = scan_excl(cg | (ce << 16), warp_sums);
-  uint32_t g_off = pre & 0xffffu, e_off = pre >> 16;
-  for (int c = 0; c < m; ++c) {
-    uint32_t gtm = 0, eqm = 0;
-#pragma unroll 8
-    for (int jj = 0; jj < 32; ++jj) {
-      const int j = (jj + lane) & 31;
-      const int i = base + c * 32 + j;
-      if (i < n) {
-        const uint32_t key = keys[i];
-        if (key > T) gtm |= 1u << j;
-        else if (key == T) eqm |= 1u << j;
-      }
+  __shared__ uint32_t w_gt[kW], w_eq[kW];
+  if (lane == 0) { w_gt[warp] = cg; w_eq[warp] = ce; }
+  __syncthreads();
+  uint32_t G = 0, E = 0;
+  for (int w = 0; w < warp; ++w) { G += w_gt[w]; E += w_eq[w]; }
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    const bool gt = i < w1 && key > T, eq = i < w1 && key == T;
+    const unsigned bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t gb = G + __popc(bg & lt), eb = E + __popc(be & lt);
+    int slot = -1;
+    if (gt) slot = (int)(gb + min(eb, need));
+    else if (eq && eb < need) slot = (int)(gb + eb);
+    if (slot >= 0) {
+      idx[slot] = i;
+      if (vals) vals[slot] = key_to_float(key);
     }
-    const uint32_t sel = gtm | eqm;
-    if (sel) {
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = (jj + lane) & 31;
-        const uint32_t bit = 1u << j, low = bit - 1u;
-        if (!(sel & bit)) continue;
-        const uint32_t gb = g_off + __popc(gtm & low), eb = e_off + __popc(eqm & low);
-        int slot = -1;
-        if (gtm & bit) slot = (int)(gb + min(eb, need));
-        else if (eb < need) slot = (int)(gb + eb);
-        if (slot >= 0) {
-          const int i = base + c * 32 + j;
-          idx[slot] = i;
-          if (vals) vals[slot] = key_to_float(keys[i]);
-        }
-      }
-    }
-    g_off += __popc(gtm);
-    e_off += __popc(eqm);
+    G += __popc(bg);
+    E += __popc(be);
   }
 }
 
