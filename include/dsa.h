@@ -26,9 +26,10 @@
  *   dsa_workspace_size() bytes.  Its first 256 bytes hold a device status word:
  *   kernels OR DSA_FLAG_* bits into it when they detect bad data (an index out
  *   of range, inconsistent cu_q/cu_k) or give up a bounded wait.  The word is
- *   sticky: clear it with dsa_clear_status() (or zero the workspace once) and
- *   read it with dsa_read_status().  The rest is scratch owned by the call
- *   while it runs; calls sharing one workspace must be stream-ordered.
+ *   sticky: clear it with dsa_clear_status() and read it with
+ *   dsa_read_status().  The rest is scratch owned by the call while it runs;
+ *   calls sharing one workspace must be stream-ordered.  Its contents between
+ *   calls are the caller's (a call never relies on earlier contents).
  * Sequences.  Query rows and key rows are packed: sequence b owns query rows
  *   cu_q[b] .. cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1, with
  *   T_b = cu_q[b+1]-cu_q[b] <= L_b = cu_k[b+1]-cu_k[b].  The queries of a

@@ -190,9 +190,20 @@ size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 
 // starts of the tensor-core schedule.  The fused forward adds the indices.
 struct IndexerScratch {
   float* scores;
+  uint32_t* hist;
   int32_t* idx;
   void* sfa;
 };
+
+// The tensor-core indexer also histograms each row for the shared-memory Top-K
+// (decode-sized problems: rows that fit shared memory, at most 4096 of them).
+bool use_topk_hist(const dsa_problem* p) {
+  return (p->idx_dtype == DSA_BF16 || p->idx_dtype == DSA_FP8_E4M3) && p->h_idx == 64 &&
+         p->d_idx == 128 && p->max_k_len <= topk_smem_max_keys() && p->total_q <= 4096;
+}
+size_t hist_bytes(const dsa_problem* p) {
+  return use_topk_hist(p) ? (size_t)p->total_q * kHistBins * 4 : 0;
+}
 
 // SFA scratch (split-row partials of the tensor-core path; 0 bytes otherwise).
 size_t sfa_scratch_bytes(const dsa_problem* p) {
@@ -203,11 +214,13 @@ size_t sfa_scratch_bytes(const dsa_problem* p) {
 size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
   const size_t o_scores = c.take(scores_bytes(p));
+  const size_t o_hist = c.take(hist_bytes(p));
   const size_t o_idx = c.take(idx_bytes(p));
   const size_t o_sfa = c.take(sfa_scratch_bytes(p));
   if (out) {
     char* b = static_cast<char*>(ws);
     out->scores = reinterpret_cast<float*>(b + o_scores);
+    out->hist = hist_bytes(p) ? reinterpret_cast<uint32_t*>(b + o_hist) : nullptr;
     out->idx = reinterpret_cast<int32_t*>(b + o_idx);
     out->sfa = b + o_sfa;
   }
@@ -270,11 +283,18 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
   carve_indexer(p, ws, &sc);
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
   const int64_t ld = scores_ld(p);
-  if (indexer_tc_eligible(ia))
+  uint32_t* hist = nullptr;
+  if (indexer_tc_eligible(ia)) {
+    ia.hist = hist = sc.hist;
+    if (hist) {
+      cudaError_t e = cudaMemsetAsync(hist, 0, hist_bytes(p), s);
+      if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "hist clear: %s", cudaGetErrorString(e));
+    }
     DSA_TRY(launch_indexer_tc(ia, sc.scores, ld, s));
-  else
+  } else {
     DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, ld, s));
-  TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws)};
+  }
+  TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws), hist};
   return run_topk(ta, s);
 }
 

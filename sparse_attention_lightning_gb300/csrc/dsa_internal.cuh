@@ -110,6 +110,7 @@ struct IndexerArgs {
   const float* q_scale;
   const float* k_scale;
   uint32_t* status;
+  uint32_t* hist = nullptr;  // tensor-core path: also fill the Top-K histogram (zero on entry)
 };
 
 int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
@@ -123,6 +124,9 @@ int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStrea
 int launch_mask_tail(const Seqs& seqs, float* scores, int64_t ld, uint32_t* status,
                      cudaStream_t stream);
 
+// Per-row histogram of score keys by their top 12 bits (order_key(s) >> 20).
+constexpr int kHistBins = 4096;
+
 struct TopkArgs {
   Seqs seqs;
   int top_k;
@@ -131,6 +135,7 @@ struct TopkArgs {
   int32_t* idx;
   float* vals;
   uint32_t* status;
+  const uint32_t* hist = nullptr;  // [total_q][kHistBins] or null
 };
 int launch_topk_rows(const TopkArgs& a, cudaStream_t stream);
 // Shared-memory-resident variant for rows of at most topk_smem_max_keys() keys.

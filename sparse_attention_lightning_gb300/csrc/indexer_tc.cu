@@ -48,7 +48,8 @@ struct Cfg {
   static constexpr int KSTEPS = FP8 ? 4 : 8;       // MMAs per tile (32 B of K each)
   static constexpr int ACC_COLS = HI;              // fp32 accumulator columns
   static constexpr int TMEM_COLS = 2 * ACC_COLS;   // double buffered
-  static constexpr int SMEM_FIXED = NS * KTILE + 2 * QTILE + 2048 /*bars etc*/ + 1024 /*align*/;
+  static constexpr int SMEM_FIXED = NS * KTILE + 2 * QTILE + kHistBins * 4 + 2048 /*bars etc*/ +
+                                    1024 /*align*/;
 };
 
 struct Params {
@@ -59,6 +60,7 @@ struct Params {
   float* scores;
   int64_t ld;
   uint32_t* status;
+  uint32_t* hist;  // [total_q][kHistBins] or null
 };
 
 __device__ __forceinline__ int64_t ftiles(int64_t n) {  // Σ_{p<n} (floor(p/128) + 1)
@@ -147,7 +149,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* ks = smem;                                  // NS key tiles
   uint8_t* qs = ks + C::NS * C::KTILE;                 // 2 query blocks
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qs + 2 * C::QTILE);
+  uint32_t* hs = reinterpret_cast<uint32_t*>(qs + 2 * C::QTILE);  // row-segment histogram
+  uint64_t* bars = reinterpret_cast<uint64_t*>(hs + kHistBins);
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* q_full = k_empty + C::NS;
@@ -155,7 +158,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   uint64_t* acc_full = q_empty + 2;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  float* wsm = reinterpret_cast<float*>(drain + 2);  // [4 epilogue warps][64]
+  uint64_t* epi_a = drain + 1;     // 128 epilogue threads: row segment scored
+  uint64_t* epi_b = drain + 2;     // 128 epilogue threads: histogram flushed
+  float* wsm = reinterpret_cast<float*>(drain + 4);  // [4 epilogue warps][64]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsm + 4 * 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* scan_ws = tmem_slot + 2;                   // [6]
@@ -188,6 +193,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (b < B) st[b] = (int32_t)(carry + excl);
     carry += tot;
   }
+  if (p.hist)
+    for (int i = threadIdx.x; i < kHistBins; i += 192) hs[i] = 0u;
   if (threadIdx.x == 0) {
     st[B] = (int32_t)carry;
     cq[B] = __ldg(p.seqs.cu_q + B);
@@ -207,6 +214,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(epi_a, 128);
+    mbar_init(epi_b, 128);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&kmap);
@@ -294,7 +303,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   } else {
     // ---------------- epilogue: warps 2..5, TMEM lane quarter warp % 4 ----------------
     const int quarter = warp & 3;
+    const int e = threadIdx.x - 64;  // 0..127
     float* wq = wsm + (warp - 2) * 64;
+    int nseg = 0;
     Cursor cur;
     cur.locate(tabs, g0);
     for (int g = g0, it = 0; g < g1; ++g, ++it) {
@@ -333,6 +344,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       if (s <= cur.pos) {
         if (FP8) sum *= __ldg(p.k_scale + cur.k0 + s);
         p.scores[(int64_t)cur.t * p.ld + s] = sum;
+        if (p.hist) atomicAdd(&hs[order_key(sum) >> 20], 1u);
+      }
+      if (p.hist && (g + 1 == g1 || cur.j + 1 == cur.ntiles)) {
+        // end of this CTA's part of the row: add the segment histogram to the row's
+        mbar_arrive(epi_a);
+        if (!__all_sync(0xffffffffu, mbar_wait(epi_a, nseg & 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) break;
+        uint32_t* grow = p.hist + (int64_t)cur.t * kHistBins;
+        for (int bin = e; bin < kHistBins; bin += 128) {
+          const uint32_t v = hs[bin];
+          if (v) { atomicAdd(grow + bin, v); hs[bin] = 0u; }
+        }
+        mbar_arrive(epi_b);
+        if (!__all_sync(0xffffffffu, mbar_wait(epi_b, nseg & 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) break;
+        ++nseg;
       }
     }
   }
@@ -362,7 +389,7 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
     return check_launch("indexer_tc: smem attribute");
   const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + C::BM - 1) / C::BM);
   const int grid = (int)(bound < num_sms() ? bound : num_sms());
-  Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status};
+  Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status, a.hist};
   DSA_LAUNCH(FP8 ? "indexer_tc_fp8" : "indexer_tc_bf16", stream,
              kern<<<grid, 192, smem, stream>>>(kmap, qmap, p));
   return check_launch("indexer_tc");

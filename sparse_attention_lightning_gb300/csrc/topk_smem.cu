@@ -7,6 +7,9 @@
 // the smaller position, written in ascending position order, -1 padded.
 // 1024 threads per row; every pass over the keys is warp-coalesced.
 //
+// When the indexer has also left a histogram of the row's scores by their top
+// 12 key bits, the threshold bin comes straight from it and only that bin's keys
+// are refined.  Otherwise:
 // The row is read once from global memory into shared memory as
 // order-preserving uint32 keys, with its min and max.  The radix select runs on
 // the offsets v = key - min, whose top 8 significant bits already spread the
@@ -26,6 +29,8 @@ constexpr int kW = kT / 32;
 constexpr int kMaxKeys = 40960;
 constexpr int kCandCap = 4096;
 constexpr size_t kSmem = sizeof(uint32_t) * ((size_t)kMaxKeys + kW * 256 + 256 + kCandCap);
+
+static_assert(kT * 4 == kHistBins, "one uint4 of histogram bins per thread");
 
 __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   extern __shared__ uint32_t sm[];
@@ -48,6 +53,44 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
     idx[j] = -1;
     if (vals) vals[j] = -INFINITY;
   }
+  // Histogram of this row's keys by their top 12 bits (filled by the indexer).
+  uint32_t hb_bin = 0, hb_above = 0, hb_cnt = 0;
+  const bool use_hist = a.hist != nullptr;
+  if (use_hist) {
+    const uint4* hrow = reinterpret_cast<const uint4*>(a.hist + (int64_t)t * kHistBins);
+    const uint4 c4 = __ldcg(hrow + tid);  // bins 4*tid .. 4*tid+3
+    if (k < n) {
+      // keys in bins above this thread's: exclusive scan in descending bin order
+      const uint32_t mine = c4.x + c4.y + c4.z + c4.w;
+      uint32_t x = mine;
+      // reverse: warp w' = kW-1-warp, lane' = 31-lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+      }
+      if (lane == 0) red_min[warp] = x;  // warp total
+      __syncthreads();
+      uint32_t above = x - mine;         // within the warp, bins of higher lanes
+      for (int w = warp + 1; w < kW; ++w) above += red_min[w];
+      if (above < (uint32_t)k && above + mine >= (uint32_t)k) {
+        const uint32_t c[4] = {c4.w, c4.z, c4.y, c4.x};  // descending bins
+        uint32_t run = above;
+        for (int i = 0; i < 4; ++i) {
+          if (run + c[i] >= (uint32_t)k) {
+            s_digit = 4 * tid + 3 - i;
+            s_above = run;
+            s_cnt = c[i];
+            break;
+          }
+          run += c[i];
+        }
+      }
+      if (tid == 0) s_ncand = 0;
+      __syncthreads();
+      hb_bin = s_digit; hb_above = s_above; hb_cnt = s_cnt;
+    }
+  }
   if (k == n) {
     for (int i = tid; i < n; i += kT) {
       idx[i] = i;
@@ -55,6 +98,7 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
     }
     return;
   }
+  const bool hist_cand = use_hist && hb_cnt <= (uint32_t)kCandCap;
 
   // --- load the row as keys, with its min and max ----------------------------
   // Vector loads, several in flight per thread (the row usually sits in L2).
@@ -88,21 +132,56 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   }
   lmin = __reduce_min_sync(0xffffffffu, lmin);
   lmax = __reduce_max_sync(0xffffffffu, lmax);
+  __syncthreads();  // (red_min was used by the histogram scan)
   if (lane == 0) { red_min[warp] = lmin; red_max[warp] = lmax; }
   __syncthreads();
   uint32_t kmin = red_min[0], kmax = red_max[0];
   for (int w = 1; w < kW; ++w) { kmin = min(kmin, red_min[w]); kmax = max(kmax, red_max[w]); }
 
   // --- radix select of the exact n-th largest key -------------------------------
-  // on offsets v = key - kmin in [0, kmax - kmin]; T = kmin + (selected offset)
-  uint32_t prefix = kmax - kmin, need = (uint32_t)k;
-  if (kmin != kmax) {
-    int hb = 31 - __clz(kmax - kmin);                     // highest bit any offset uses
-    uint32_t mask = hb == 31 ? 0u : ~((2u << hb) - 1u);   // bits zero in every offset
-    prefix = 0u;
-    const uint32_t* src = keys;
-    int src_n = n;
-    bool compacted = false;
+  // Without a histogram: on offsets v = key - kmin in [0, kmax - kmin], T = kmin +
+  // (selected offset).  With one: the top 12 bits are already fixed by the threshold
+  // bin, and only the keys of that bin (compacted here when they fit) are searched.
+  uint32_t prefix, need, mask;
+  int hb;
+  const uint32_t* src = keys;
+  int src_n = n;
+  bool compacted = false, done = false;
+  if (use_hist) {
+    kmin = 0u;
+    prefix = hb_bin << 20;
+    mask = 0xfff00000u;
+    need = (uint32_t)k - hb_above;
+    hb = 19;
+    if (hist_cand) {
+      for (int i0 = 0; i0 < n; i0 += kT) {
+        const int i = i0 + tid;
+        const uint32_t key = i < n ? keys[i] : 0u;
+        const bool hitk = i < n && (key & mask) == prefix;
+        const unsigned bal = __ballot_sync(0xffffffffu, hitk);
+        uint32_t wbase = 0;
+        if (lane == 0 && bal) wbase = atomicAdd(&s_ncand, (uint32_t)__popc(bal));
+        wbase = __shfl_sync(0xffffffffu, wbase, 0);
+        if (hitk) cand[wbase + __popc(bal & ((1u << lane) - 1u))] = key;
+      }
+      __syncthreads();
+      src = cand;
+      src_n = (int)s_ncand;
+      compacted = true;
+    }
+  } else {
+    prefix = kmax - kmin;
+    need = (uint32_t)k;
+    mask = 0u;
+    hb = 0;
+    done = kmin == kmax;
+    if (!done) {
+      hb = 31 - __clz(kmax - kmin);                  // highest bit any offset uses
+      mask = hb == 31 ? 0u : ~((2u << hb) - 1u);     // bits zero in every offset
+      prefix = 0u;
+    }
+  }
+  if (!done) {
     while (true) {
       const int shift = hb >= 7 ? hb - 7 : 0;
       const int nb = hb - shift + 1;
@@ -155,6 +234,7 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
       if (shift == 0) break;
       hb = shift - 1;
       if (!compacted && cnt <= (uint32_t)kCandCap) {
+        __syncthreads();
         if (tid == 0) s_ncand = 0;
         __syncthreads();
         for (int i0 = 0; i0 < n; i0 += kT) {  // one counter update per warp
