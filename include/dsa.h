@@ -150,7 +150,8 @@ int dsa_topk(const dsa_problem* p, const float* scores, int64_t ld, int32_t* idx
  * LLMs" §4.1 fused_indexer(q_idx, k_cache, head_weights, top_k); "Optimizing
  * LLM Inference for New Architectures", §3: only the final Top-K indices leave
  * the operator).  Arguments and results are those of dsa_indexer_scores
- * followed by dsa_topk.
+ * followed by dsa_topk, except that the selected positions of a row may come
+ * in any (deterministic) order: valid entries first, then -1 padding.
  */
 int dsa_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx,
                       const float* w, const float* q_scale, const float* k_scale,

@@ -1,7 +1,7 @@
 """Comparison rules between the CUDA path and the fp64 oracle.
 
 Top-K: the GPU row must hold exactly n = min(k, pos+1) unique causal positions
-(ascending, then -1 padding); every position in the symmetric difference with
+first, then -1 padding (their order is free); every position in the symmetric difference with
 the oracle's set must have an oracle score within 1e-3 (relative) of the
 oracle's n-th score.  Scores: max |gpu - oracle| <= 1e-2 · max |oracle| per row.
 Attention: compared with the oracle's SFA evaluated on the GPU's own index set:
@@ -37,7 +37,7 @@ def check_topk_row(gpu_row: np.ndarray, scores: np.ndarray, k: int, ctx: str = "
     valid = gpu_row[:n]
     assert np.all(gpu_row[n:] == -1), f"{ctx}: padding is not -1"
     assert np.all(valid >= 0) and np.all(valid <= pos), f"{ctx}: non-causal index"
-    assert np.all(np.diff(valid) > 0), f"{ctx}: indices not unique ascending"
+    assert np.unique(valid).size == valid.size, f"{ctx}: repeated index"
     order = np.argsort(-scores, kind="stable")
     ref = order[:n]
     s_k = scores[order[n - 1]]
