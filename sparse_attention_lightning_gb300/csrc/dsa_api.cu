@@ -197,16 +197,15 @@ struct IndexerScratch {
   void* sfa;
 };
 
-// The tensor-core indexer also histograms each row for the segmented Top-K
-// (decode-sized problems: at most 4096 rows).
+// The tensor-core indexer also histograms each row for the segmented Top-K.
 bool use_topk_hist(const dsa_problem* p) {
   return (p->idx_dtype == DSA_BF16 || p->idx_dtype == DSA_FP8_E4M3) && p->h_idx == 64 &&
-         p->d_idx == 128 && p->max_k_len <= topk_seg_max_keys() && p->total_q <= 4096;
+         p->d_idx == 128 && p->max_k_len <= topk_seg_max_keys() && p->num_seqs <= 4096;
 }
 size_t hist_bytes(const dsa_problem* p) {
   return use_topk_hist(p) ? (size_t)p->total_q * (kHistBins + 1) * 4 : 0;
 }
-int64_t segbuf_ld(const dsa_problem* p) { return (int64_t)topk_seg_segments(p->max_k_len) * 4096; }
+int64_t segbuf_ld(const dsa_problem* p) { return (int64_t)topk_seg_segments(p->max_k_len) * 8192; }
 size_t segbuf_bytes(const dsa_problem* p) {
   return use_topk_hist(p) ? (size_t)p->total_q * segbuf_ld(p) * 4 : 0;
 }

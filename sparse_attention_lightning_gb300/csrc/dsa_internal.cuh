@@ -142,7 +142,7 @@ int launch_topk_rows(const TopkArgs& a, cudaStream_t stream);
 int topk_smem_max_keys();
 int launch_topk_smem(const TopkArgs& a, cudaStream_t stream);
 // Segmented multi-CTA variant (needs a.hist): buf [total_q][buf_ld] int32 with
-// buf_ld = 4096 * topk_seg_segments(max_k_len), seg_counts [total_q][segments][2],
+// buf_ld = 8192 * topk_seg_segments(max_k_len), seg_counts [total_q][segments][2],
 // done [total_q] zero on entry (left zero).
 int topk_seg_segments(int max_k_len);
 int topk_seg_max_keys();

@@ -544,12 +544,17 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
             for (int c = 0; c < 8; ++c)
               bulk_load(po2 + c * 1024, p.part_o + other * (64 * kH) + c * 1024, 16384, drain + 1);
           }
+          // merged in split order (split 0 first), whichever split runs the merge, so the
+          // result does not depend on which one finished last
           const float mo = __ldcg(p.part_ml + (other * kH + h) * 2);
           const float lo2 = __ldcg(p.part_ml + (other * kH + h) * 2 + 1);
-          const float M = fmaxf(m_ref, mo);
-          const float wa = l > 0.f ? ex2(m_ref - M) : 0.f;
-          const float wb = lo2 > 0.f ? ex2(mo - M) : 0.f;
-          const float wsum = wa * l + wb * lo2;
+          const bool first = sp == 0;
+          const float m0 = first ? m_ref : mo, l0 = first ? l : lo2;
+          const float m1 = first ? mo : m_ref, l1 = first ? lo2 : l;
+          const float M = fmaxf(m0, m1);
+          const float w0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
+          const float w1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
+          const float wsum = w0 * l0 + w1 * l1;
           const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
           if (!__all_sync(0xffffffffu, mbar_wait(drain + 1, 0, abort_flag, p.status,
                                                  DSA_FLAG_TIMEOUT))) break;
@@ -563,10 +568,13 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 x = po2[(8 * b + i) * kH + h];
-              o[4 * i] = (wa * __uint_as_float(r[4 * i]) + wb * x.x) * inv;
-              o[4 * i + 1] = (wa * __uint_as_float(r[4 * i + 1]) + wb * x.y) * inv;
-              o[4 * i + 2] = (wa * __uint_as_float(r[4 * i + 2]) + wb * x.z) * inv;
-              o[4 * i + 3] = (wa * __uint_as_float(r[4 * i + 3]) + wb * x.w) * inv;
+              const float xo[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float own = __uint_as_float(r[4 * i + e]);
+                const float a0 = first ? own : xo[e], a1 = first ? xo[e] : own;
+                o[4 * i + e] = (w0 * a0 + w1 * a1) * inv;
+              }
             }
             store_block(o, p.out_f32, p.out, row0, colbase + 32 * b, stage, lane);
           }

@@ -7,7 +7,7 @@
 // n = min(top_k, pos+1) largest of scores[t, 0..pos]; equal scores go to the
 // smaller position.
 //
-// Phase 1, one CTA per 4096-key segment of a row: the histogram gives the bin
+// Phase 1, one CTA per 8192-key segment of a row: the histogram gives the bin
 // B* that holds the n-th largest key and the count of keys above it.  The CTA
 // reads its keys once and, in position order (block-wide prefix sums, no
 // atomics), writes the positions of keys in bins above B* ("definite") and of
@@ -23,9 +23,9 @@ namespace {
 
 constexpr int kT = 1024;
 constexpr int kW = kT / 32;
-constexpr int kSeg = 4 * kT;       // keys per segment CTA
+constexpr int kSeg = 8 * kT;       // keys per segment CTA
 constexpr int kCandCap = 6144;     // candidates refined from shared memory
-constexpr int kMaxSegs = 1024;     // segments per row (rows up to 4M keys)
+constexpr int kMaxSegs = 512;      // segments per row (rows up to 4M keys)
 
 struct Shared {
   uint32_t warp_a[kW], warp_b[kW];
@@ -127,21 +127,25 @@ __global__ void __launch_bounds__(kT, 1) topk_seg_kernel(TopkArgs a, int32_t* bu
   // ---- phase 1: this segment's definite positions and candidates ----
   threshold_bin(a.hist + (int64_t)t * kHistBins, (uint32_t)k, S);
   const uint32_t bstar = S.s_bin;
-  const int i0 = s0 + 4 * tid;
-  uint32_t key[4];
+  const int i0 = s0 + 8 * tid;  // this thread's 8 consecutive keys
+  uint32_t key[8];
   {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i0 + 3 < n) f = __ldcg(reinterpret_cast<const float4*>(row + i0));
-    else {
-      if (i0 < n) f.x = row[i0];
-      if (i0 + 1 < n) f.y = row[i0 + 1];
-      if (i0 + 2 < n) f.z = row[i0 + 2];
-    }
-    key[0] = order_key(f.x); key[1] = order_key(f.y); key[2] = order_key(f.z); key[3] = order_key(f.w);
-  }
-  uint32_t dm = 0, cm = 0;  // 4-bit masks
+    float f[8];
+    if (i0 + 7 < n) {
+      const float4 a4 = __ldcg(reinterpret_cast<const float4*>(row + i0));
+      const float4 b4 = __ldcg(reinterpret_cast<const float4*>(row + i0 + 4));
+      f[0] = a4.x; f[1] = a4.y; f[2] = a4.z; f[3] = a4.w;
+      f[4] = b4.x; f[5] = b4.y; f[6] = b4.z; f[7] = b4.w;
+    } else {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) f[j] = i0 + j < n ? row[i0 + j] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) key[j] = order_key(f[j]);
+  }
+  uint32_t dm = 0, cm = 0;  // 8-bit masks
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
     if (i0 + j < n) {
       const uint32_t b = key[j] >> 20;
       if (b > bstar) dm |= 1u << j;
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kT, 1) topk_seg_kernel(TopkArgs a, int32_t* bu
   {
     uint32_t pd = pre & 0xffffu, pc = (pre >> 16) + (kSeg - tcn);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       if (dm >> j & 1u) sbuf[pd++] = i0 + j;
       if (cm >> j & 1u) sbuf[pc++] = i0 + j;
     }

@@ -59,10 +59,22 @@ def test_static_scratch_entry_point_matches_workspace_entry_point():
         assert int(flags[0]) == 0
         a, b = idx.cpu().numpy(), ref_idx.cpu().numpy()
         va, vb = vals.cpu().numpy(), ref_vals.cpu().numpy()
-        assert np.array_equal(a, b)
-        fin = np.isfinite(vb)
-        assert np.array_equal(np.isfinite(va), fin)
-        assert np.abs(va[fin] - vb[fin]).max(initial=0.0) <= 1e-2 * np.abs(vb[fin]).max(initial=1)
+        for t in range(cfg.total_q):
+            # same selected set, up to swaps of positions whose scores sit within 1e-3
+            # (relative) of the k-th score; the order inside a row is free
+            sa = dict(zip(a[t][a[t] >= 0].tolist(), va[t][a[t] >= 0].tolist()))
+            sb = dict(zip(b[t][b[t] >= 0].tolist(), vb[t][b[t] >= 0].tolist()))
+            assert len(sa) == len(sb) == (a[t] >= 0).sum() == (b[t] >= 0).sum()
+            assert np.all(a[t][len(sa):] == -1) and np.all(b[t][len(sb):] == -1)
+            kth = min(sb.values())
+            for p_, v_ in list(set(sa.items()) - set(sb.items())):
+                if p_ in sb:  # same position: scores agree to the score tolerance
+                    assert abs(v_ - sb[p_]) <= 1e-2 * max(abs(x) for x in sb.values())
+                else:
+                    assert abs(v_ - kth) <= 1e-3 * abs(kth), (t, p_, v_, kth)
+            for p_, v_ in sb.items():
+                if p_ not in sa:
+                    assert abs(v_ - kth) <= 1e-3 * abs(kth), (t, p_, v_, kth)
 
 
 def test_static_scratch_rejects_oversized_problems():
