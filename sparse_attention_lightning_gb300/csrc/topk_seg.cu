@@ -25,7 +25,7 @@ constexpr int kT = 1024;
 constexpr int kW = kT / 32;
 constexpr int kSeg = 8 * kT;       // keys per segment CTA
 constexpr int kCandCap = 6144;     // candidates refined from shared memory
-constexpr int kMaxSegs = 512;      // segments per row (rows up to 4M keys)
+constexpr int kMaxSegs = 512;      // segments per row (rows up to 4M keys; grid y <= 65535)
 
 struct Shared {
   uint32_t warp_a[kW], warp_b[kW];
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kT, 1) topk_seg_kernel(TopkArgs a, int32_t* bu
                                                          uint32_t* done) {
   extern __shared__ uint8_t smem_raw[];
   Shared& S = *reinterpret_cast<Shared*>(smem_raw);
-  const int seg = blockIdx.x, t = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  const int t = blockIdx.x, seg = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
   RowInfo r;
   if (!query_row_info(a.seqs, t, r, a.status)) return;
   const int n = r.pos + 1;
@@ -299,7 +299,7 @@ int launch_topk_seg(const TopkArgs& a, int32_t* buf, int64_t buf_ld, uint32_t* s
   if (cudaFuncSetAttribute(topk_seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return check_launch("topk_seg: smem attribute");
-  dim3 grid(nseg, a.seqs.total_q);
+  dim3 grid(a.seqs.total_q, nseg);  // rows on x (up to 2^31 - 1), segments on y
   DSA_LAUNCH("topk_seg", stream,
              topk_seg_kernel<<<grid, kT, smem, stream>>>(a, buf, buf_ld, seg_counts, nseg, done));
   return check_launch("topk_seg");
