@@ -20,7 +20,7 @@
 // distributed shared memory (same order in both CTAs, so both hold identical
 // logits and take identical softmax decisions).  Each CTA then multiplies P by its
 // own 256 value columns: O_half (128 x 256 fp32) lives in TMEM next to a
-// double-buffered 128 x 64 S tile.
+// double-buffered 128 x 64 S tile and the 128 x 64 bf16 P tile.
 //
 // Per chunk of 64 selected rows:
 //  * producer warp: the 16-byte pieces of the CTA's columns of the 64 rows go
@@ -29,11 +29,14 @@
 //  * MMA thread: S = Q_half · KV_half^T (M=128, N=64, K=256|320, K-major), then,
 //    once P is ready, O += P · V (M=128, N=256, K=64, V read MN-major straight
 //    from the gathered tile);
-//  * softmax warps (one thread per head): read S from TMEM, push their partial
+//  * softmax warps (two warpgroups, a thread per head and half of the chunk's
+//    64 columns; the halves combine their maxima through shared memory): read S
+//    from TMEM, push their partial
 //    into the peer CTA's shared memory with st.async (coalesced asynchronous
 //    remote stores that complete on the peer's mbarrier), read the peer's from
 //    their own, keep a running max (O is rescaled only when the max
-//    grows by more than 2^8), write P = 2^(x - m) as bf16 for the PV MMA.
+//    grows by more than 2^8), write P = 2^(x - m) as bf16 into TMEM, where the
+//    P·V MMA reads it as its A operand.
 //
 // Decode rows are split over 2 clusters when there are few queries; the second
 // cluster of a row to finish merges the other's partial (O, max, sum) into its own.
@@ -54,12 +57,13 @@ constexpr int kNAmax = 5;      // 128-byte column atoms of the larger half
 constexpr int kQBytes = kNAmax * kH * 128;    // 80 KB
 constexpr int kKVStage = kNAmax * kNC * 128;  // 40 KB
 constexpr int kStages = 2;
-constexpr int kPBytes = kH * kNC * 2;         // 16 KB
 constexpr int kXBytes = kH * kNC * 4;         // 32 KB
 constexpr int kMaxTopK = 2048;
-constexpr int kSmem = kQBytes + kStages * kKVStage + kPBytes + kXBytes + kMaxTopK * 4 + 1024 + 1024;
-constexpr int kTmemCols = 512;                // S0 [0,64) S1 [64,128) O [128,384)
+constexpr int kThreads = 320;                 // producer, MMA, 8 softmax warps
+constexpr int kSmem = kQBytes + kStages * kKVStage + kXBytes + kMaxTopK * 4 + 4096 + 1024;
+constexpr int kTmemCols = 512;                // S0 [0,64) S1 [64,128) O [128,384) P [384,416)
 constexpr int kOCol = 128;
+constexpr int kPCol = 384;                    // P (bf16, 2 per column) for the P·V MMA
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows > 2^8
 
 struct Params {
@@ -110,53 +114,13 @@ __device__ __forceinline__ int seq_of_row(const Seqs& s, int t, int lane) {
   return lo;
 }
 
-// Output of 32 consecutive columns of every head of a warp, staged through
-// shared memory so each store instruction writes whole row segments.
-__device__ __forceinline__ void store_block(const float (&v)[32], int out_f32, void* out,
-                                            int64_t row0, int col0, uint8_t* stage, int lane) {
-  if (out_f32) {  // 32 rows x 128 B
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<float4*>(stage + lane * 128 + ((j ^ (lane & 7)) * 16)) =
-          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = i * 4 + (lane >> 3), j = lane & 7;
-      const float4 x = *reinterpret_cast<const float4*>(stage + r * 128 + ((j ^ (r & 7)) * 16));
-      reinterpret_cast<float4*>(static_cast<float*>(out) + (row0 + r) * kDC + col0)[j] = x;
-    }
-  } else {        // 32 rows x 64 B
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
-        w[e] = *reinterpret_cast<const uint32_t*>(&b2);
-      }
-      *reinterpret_cast<uint4*>(stage + lane * 64 + ((j ^ (lane & 3)) * 16)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = i * 8 + (lane >> 2), j = lane & 3;
-      const uint4 x = *reinterpret_cast<const uint4*>(stage + r * 64 + ((j ^ (r & 3)) * 16));
-      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + (row0 + r) * kDC + col0)[j] = x;
-    }
-  }
-  __syncwarp();
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* qs = smem;
   uint8_t* kvs = qs + kQBytes;
-  uint8_t* ps = kvs + kStages * kKVStage;
-  float4* xs = reinterpret_cast<float4*>(ps + kPBytes);  // [16][128]: peer's partial logits
+  float4* xs = reinterpret_cast<float4*>(kvs + kStages * kKVStage);  // [16][128]: peer's logits
   int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + kXBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(list + kMaxTopK);
   uint64_t* kv_full = bars;          // [2]  32 producer lanes (cp.async completion)
@@ -177,8 +141,10 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
   int* s_last = reinterpret_cast<int*>(bars + 22);
-  uint64_t* sync_a = bars + 23;      // 128 softmax threads: partials written
+  uint64_t* sync_a = bars + 23;      // 256 softmax threads: partials written
   uint64_t* sync_b = bars + 24;      // the arrival count has been taken
+  uint64_t* hsync = bars + 25;       // the 8 softmax warps: per-head halves exchanged
+  float* mx = reinterpret_cast<float*>(bars + 26);  // [2 phases][2 halves][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -191,16 +157,17 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 32); mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
+      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 8);
     }
     mbar_init(q_full, 1); mbar_init(q_empty, 1);
-    mbar_init(p_full, 4); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
-    mbar_init(x_full, 1); mbar_init(x_empty, 4);
-    mbar_init(meta_full, 1); mbar_init(meta_empty, 5);
+    mbar_init(p_full, 8); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
+    mbar_init(x_full, 1); mbar_init(x_empty, 8);
+    mbar_init(meta_full, 1); mbar_init(meta_empty, 9);
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
-    mbar_init(sync_a, 128);
+    mbar_init(sync_a, 256);
     mbar_init(sync_b, 1);
+    mbar_init(hsync, 8);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&qmap);
@@ -309,7 +276,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(kH, kNC);                  // K-major A and B
       const uint32_t idesc_pv = idesc_bf16(kH, 256, false, true);    // V is MN-major
-      const uint32_t qa = smem_u32(qs), kv0 = smem_u32(kvs), p0 = smem_u32(ps);
+      const uint32_t qa = smem_u32(qs), kv0 = smem_u32(kvs);
       int gc = 0;
       bool stop = false;
       auto pv = [&](int g, int first) -> bool {
@@ -317,10 +284,10 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
         tc_fence_after();
         const uint32_t vb = kv0 + (g & 1) * kKVStage;
 #pragma unroll
-        for (int kk = 0; kk < kNC / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(p0 + kk * 32, 16, 1024);
+        for (int kk = 0; kk < kNC / 16; ++kk) {  // P from TMEM: 16 rows = 8 columns per step
           const uint64_t bd = sdesc_sw128(vb + kk * 2048, kNC * 128, 1024);
-          mma_bf16(tmem + kOCol, ad, bd, idesc_pv, (first == 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, bd, idesc_pv,
+                      (first == 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&kv_empty[g & 1]);
         mma_commit(p_empty);
@@ -366,17 +333,29 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
       mbar_wait_drain(drain, 0);
     }
   } else {
-    // ---------------- softmax / epilogue: one thread per head ----------------
+    // ---------------- softmax / epilogue: 2 warpgroups; thread = (head, half of the chunk) ----
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;        // warps 2..5: columns 0..31, warps 6..9: 32..63
     const int h = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t xs_peer = mapa(smem_u32(xs), peer);  // our partial goes there
     const uint32_t x_full_peer = mapa(smem_u32(x_full), peer);
     const uint32_t x_empty_peer = mapa(smem_u32(x_empty), peer);
-    uint8_t* prow = ps + h * 128;
-    uint8_t* stage = ps + quarter * 4096;  // output staging (P is idle between units)
-    int gc = 0;
+    const bool leader = threadIdx.x == 64;
+    int gc = 0, nsync = 0;
     bool stop = false;
+    // combine a per-head value with the other half's (bounded 8-warp exchange)
+    auto exchange = [&](float v) -> float {
+      float* slot = mx + (nsync & 1) * 256;
+      slot[half * 128 + h] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hsync);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(hsync, nsync & 1, abort_flag, p.status,
+                                                        DSA_FLAG_TIMEOUT));
+      ++nsync;
+      if (!ok) { stop = true; return 0.f; }
+      return slot[(1 - half) * 128 + h];
+    };
     for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
       if (!__all_sync(0xffffffffu, mbar_wait(meta_full, ui & 1, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT))) break;
@@ -386,50 +365,46 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
       const int t = u / p.nsplit, sp = u - t * p.nsplit;
       const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
       const int n = hi - lo, nch = (n + kNC - 1) / kNC;
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the sum
       for (int c = 0; c < nch; ++c, ++gc) {
         const int sb = gc & 1;
         const int rows_in = min(kNC, n - c * kNC);
         if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gc >> 1) & 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) { stop = true; break; }
         tc_fence_after();
-        float s[kNC];
+        float s[32];
         {
           uint32_t r[32];
-          tmem_ld32(lane_base + sb * kNC, r);
+          tmem_ld32(lane_base + sb * kNC + 32 * half, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
-          tmem_ld32(lane_base + sb * kNC + 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[sb]);
         // exchange the partial logits: st.async ours into the peer's buffer ([16][128]
-        // float4, so a warp's stores are contiguous; the bytes complete on the peer's
-        // x_full), then read the peer's from our own buffer
-        if (threadIdx.x == 64) mbar_arrive_expect_tx(x_full, kXBytes);
+        // float4; the bytes complete on the peer's x_full), read the peer's from ours
+        if (leader) mbar_arrive_expect_tx(x_full, kXBytes);
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_empty, (gc & 1) ^ 1, abort_flag,
                                                        p.status, DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
 #pragma unroll
-        for (int q = 0; q < kNC / 4; ++q)
-          st_async_f4(xs_peer + (uint32_t)((q * kH + h) * 16),
+        for (int q = 0; q < 8; ++q)
+          st_async_f4(xs_peer + (uint32_t)(((8 * half + q) * kH + h) * 16),
                       make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]), x_full_peer);
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_full, gc & 1, abort_flag, p.status,
                                                        DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
-        float4 xo[kNC / 4];
+        float4 xo[8];
 #pragma unroll
-        for (int q = 0; q < kNC / 4; ++q) xo[q] = xs[q * kH + h];
+        for (int q = 0; q < 8; ++q) xo[q] = xs[(8 * half + q) * kH + h];
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(x_empty_peer);  // our buffer may be refilled
         float m_c = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kNC / 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
           const float other[4] = {xo[q].x, xo[q].y, xo[q].z, xo[q].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -437,10 +412,12 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
             const float lo_part = rank ? other[e] : s[i];
             const float hi_part = rank ? s[i] : other[e];
             const float x = (lo_part + hi_part) * p.scale_log2;
-            s[i] = i < rows_in ? x : -INFINITY;
+            s[i] = 32 * half + i < rows_in ? x : -INFINITY;
             m_c = fmaxf(m_c, s[i]);
           }
         }
+        m_c = fmaxf(m_c, exchange(m_c));
+        if (stop) break;
         // running max: move the reference only when it grows by more than 2^8
         const bool grow = m_c > m_ref + kRescaleLog2;
         const float m_new = grow ? m_c : m_ref;
@@ -450,19 +427,20 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
           if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status,
                                                  DSA_FLAG_TIMEOUT))) { stop = true; break; }
           tc_fence_after();
-          for (int b = 0; b < 8; ++b) {
+          for (int b = 0; b < 4; ++b) {  // this half's 128 output columns
             uint32_t r[32];
-            tmem_ld32(lane_base + kOCol + 32 * b, r);
+            const uint32_t ta = lane_base + kOCol + 128 * half + 32 * b;
+            tmem_ld32(ta, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * factor);
-            tmem_st32(lane_base + kOCol + 32 * b, r);
+            tmem_st32(ta, r);
           }
           tc_fence_before();
         }
         m_ref = m_new;
-        uint32_t pk[kNC / 2];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < kNC / 2; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(s[2 * i] - m_ref),
                                                           ex2(s[2 * i + 1] - m_ref));
           const float2 f2 = __bfloat1622float2(b2);
@@ -471,11 +449,9 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
         }
         if (!__all_sync(0xffffffffu, mbar_wait(p_empty, (gc & 1) ^ 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) { stop = true; break; }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(prow + ((j ^ (h & 7)) * 16)) =
-              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        fence_proxy_async_smem();
+        tc_fence_after();
+        tmem_st16(lane_base + kPCol + 16 * half, pk);
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
       }
@@ -488,44 +464,68 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
                                                DSA_FLAG_TIMEOUT))) break;
         tc_fence_after();
       }
-      const int64_t row0 = (int64_t)t * kH + quarter * 32;  // first head row of this warp
+      const float lo_sum = exchange(l);  // the other half's share
+      if (stop) break;
+      const float ltot = half == 0 ? l + lo_sum : lo_sum + l;  // same order in both halves
+      const int ocol = 128 * half;     // this thread's 128 output columns (of the CTA's 256)
       if (p.nsplit == 1) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        for (int b = 0; b < 8; ++b) {
+        const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+        uint8_t* orow = static_cast<uint8_t*>(p.out) +
+                        (((int64_t)t * kH + h) * kDC + colbase + ocol) * (p.out_f32 ? 4 : 2);
+        for (int b = 0; b < 4; ++b) {
           uint32_t r[32];
-          if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
+          if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
           else
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
-          float o[32];
+          if (p.out_f32) {
+            float4* o = reinterpret_cast<float4*>(orow) + 8 * b;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]) * inv;
-          store_block(o, p.out_f32, p.out, row0, colbase + 32 * b, stage, lane);
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                 __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(orow) + 4 * b;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
+                                                                __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
+                w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
         }
-        if (rank == 0 && p.lse)
-          p.lse[(int64_t)t * kH + h] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (rank == 0 && half == 0 && p.lse)
+          p.lse[(int64_t)t * kH + h] =
+              ltot > 0.f ? (m_ref + log2f(ltot)) * 0.69314718055994531f : -INFINITY;
       } else {
         // split of a row: publish (O, m, l); the second split of the row to finish merges
         const int64_t slot = ((int64_t)t * p.nsplit + sp) * 2 + rank;
         float4* po = p.part_o + slot * (64 * kH);
-        for (int b = 0; b < 8; ++b) {
+        for (int b = 0; b < 4; ++b) {
           uint32_t r[32];
-          if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
+          if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
           else
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            po[(8 * b + i) * kH + h] =
+            po[(32 * half + 8 * b + i) * kH + h] =
                 make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
         }
-        p.part_ml[(slot * kH + h) * 2] = m_ref;
-        p.part_ml[(slot * kH + h) * 2 + 1] = l;
-        // all 128 partial rows are out before the arrival count moves (bounded waits)
+        if (half == 0) {
+          p.part_ml[(slot * kH + h) * 2] = m_ref;
+          p.part_ml[(slot * kH + h) * 2 + 1] = ltot;
+        }
+        // all 256 partial rows are out before the arrival count moves (bounded waits)
         __threadfence();
         mbar_arrive(sync_a);
-        if (threadIdx.x == 64) {
+        if (leader) {
           const bool okw = mbar_wait(sync_a, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT);
           *s_last = okw && atomicAdd(p.counters + t * 2 + rank, 1) == p.nsplit - 1;
           mbar_arrive(sync_b);
@@ -534,11 +534,11 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
                                                DSA_FLAG_TIMEOUT))) break;
         if (*s_last) {
           // The other split's (O, m, l) of this column half: one bulk copy of its
-          // 128 KB into the (now idle) query/KV area, then each thread merges its head.
+          // 128 KB into the (now idle) query/KV area, then each thread merges.
           __threadfence();
           const int64_t other = ((int64_t)t * p.nsplit + (1 - sp)) * 2 + rank;
           float4* po2 = reinterpret_cast<float4*>(qs);
-          if (threadIdx.x == 64) {
+          if (leader) {
             fence_proxy_async_all();
             mbar_arrive_expect_tx(drain + 1, kH * 256 * 4);
             for (int c = 0; c < 8; ++c)
@@ -549,8 +549,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
           const float mo = __ldcg(p.part_ml + (other * kH + h) * 2);
           const float lo2 = __ldcg(p.part_ml + (other * kH + h) * 2 + 1);
           const bool first = sp == 0;
-          const float m0 = first ? m_ref : mo, l0 = first ? l : lo2;
-          const float m1 = first ? mo : m_ref, l1 = first ? lo2 : l;
+          const float m0 = first ? m_ref : mo, l0 = first ? ltot : lo2;
+          const float m1 = first ? mo : m_ref, l1 = first ? lo2 : ltot;
           const float M = fmaxf(m0, m1);
           const float w0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
           const float w1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
@@ -558,16 +558,18 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
           const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
           if (!__all_sync(0xffffffffu, mbar_wait(drain + 1, 0, abort_flag, p.status,
                                                  DSA_FLAG_TIMEOUT))) break;
-          for (int b = 0; b < 8; ++b) {
+          uint8_t* orow = static_cast<uint8_t*>(p.out) +
+                          (((int64_t)t * kH + h) * kDC + colbase + ocol) * (p.out_f32 ? 4 : 2);
+          for (int b = 0; b < 4; ++b) {
             uint32_t r[32];
-            if (have) tmem_ld32(lane_base + kOCol + 32 * b, r);
+            if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
             else
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = 0u;
             float o[32];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float4 x = po2[(8 * b + i) * kH + h];
+              const float4 x = po2[(32 * half + 8 * b + i) * kH + h];
               const float xo[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -576,9 +578,26 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
                 o[4 * i + e] = (w0 * a0 + w1 * a1) * inv;
               }
             }
-            store_block(o, p.out_f32, p.out, row0, colbase + 32 * b, stage, lane);
+            if (p.out_f32) {
+              float4* op = reinterpret_cast<float4*>(orow) + 8 * b;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                op[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            } else {
+              uint4* op = reinterpret_cast<uint4*>(orow) + 4 * b;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * i + 2 * e], o[8 * i + 2 * e + 1]);
+                  w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                op[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            }
           }
-          if (rank == 0 && p.lse)
+          if (rank == 0 && half == 0 && p.lse)
             p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f
                                                     : -INFINITY;
         }
@@ -647,7 +666,8 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   const int64_t units = (int64_t)a.seqs.total_q * ns;
   const int max_clusters = num_sms() / 2;
   const int clusters = (int)(units < max_clusters ? units : max_clusters);
-  DSA_LAUNCH("sfa_tc", stream, sfa_tc_kernel<<<2 * clusters, 192, kSmem, stream>>>(qmap, p));
+  DSA_LAUNCH("sfa_tc", stream,
+             sfa_tc_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(qmap, p));
   return check_launch("sfa_tc");
 }
 
