@@ -12,31 +12,34 @@
 //
 // Why a CTA pair.  All 128 heads share each gathered latent row, so heads are
 // the MMA's M = 128.  A single CTA would need the whole query block (128 x 576
-// bf16 = 144 KB of shared memory) and a 128 x 512 fp32 output accumulator, which
-// is all 512 TMEM columns with no room for the logits.  So a 2-CTA cluster splits
-// the columns: CTA 0 owns latent columns 0..255, CTA 1 owns latent 256..511 plus
-// the 64 rope columns.  Each CTA gathers only its columns of every selected row,
-// computes a partial S over them, and the two partial S tiles are added through
-// distributed shared memory (same order in both CTAs, so both hold identical
-// logits and take identical softmax decisions).  Each CTA then multiplies P by its
-// own 256 value columns: O_half (128 x 256 fp32) lives in TMEM next to a
-// double-buffered 128 x 64 S tile and the 128 x 64 bf16 P tile.
+// bf16 = 144 KB) and a 128 x 512 fp32 output accumulator, which is all 512 TMEM
+// columns with no room for the logits.  So a 2-CTA cluster splits the work:
+//  * logits: CTA 0 takes columns 0..287, CTA 1 columns 288..575 (18 K-steps
+//    each); each computes a partial S over its columns and the two partial S
+//    tiles are added through distributed shared memory, in the same order in both
+//    CTAs, so both hold identical logits and take identical softmax decisions;
+//  * values: CTA 0 accumulates output columns 0..255, CTA 1 columns 256..511.
+// So CTA 0 gathers columns 0..287 of every selected row and CTA 1 columns
+// 256..575.  The CTA's 288 query columns live in TMEM (the logit MMA reads its A
+// operand from there), which leaves shared memory to a 3-stage ring of gathered
+// rows and a double exchange buffer.  TMEM: O (128 x 256 fp32) | Q (144 columns
+// of bf16 pairs) | S (128 x 64 fp32) | P (64 bf16 per head).
 //
 // Per chunk of 64 selected rows:
-//  * producer warp: the 16-byte pieces of the CTA's columns of the 64 rows go
-//    straight into the 128-byte-swizzled operand layout with cp.async (one warp
-//    instruction moves 4 rows x 128 B); completion arrives on an mbarrier;
-//  * MMA thread: S = Q_half · KV_half^T (M=128, N=64, K=256|320, K-major), then,
-//    once P is ready, O += P · V (M=128, N=256, K=64, V read MN-major straight
-//    from the gathered tile);
-//  * softmax warps (two warpgroups, a thread per head and half of the chunk's
-//    64 columns; the halves combine their maxima through shared memory): read S
-//    from TMEM, push their partial
-//    into the peer CTA's shared memory with st.async (coalesced asynchronous
-//    remote stores that complete on the peer's mbarrier), read the peer's from
-//    their own, keep a running max (O is rescaled only when the max
-//    grows by more than 2^8), write P = 2^(x - m) as bf16 into TMEM, where the
-//    P·V MMA reads it as its A operand.
+//  * two producer warps (32 rows each): the 16-byte pieces of the CTA's columns
+//    go straight into the 128-byte-swizzled operand layout with cp.async;
+//    completion arrives on the stage's mbarrier;
+//  * MMA thread: S = Q_cols · KV_cols^T (M=128, N=64, K=288; A from TMEM, B
+//    K-major in shared memory), then, once P is ready, O += P · V (M=128, N=256,
+//    K=64; P from TMEM, V read MN-major straight from the gathered tile);
+//  * softmax warps (two warpgroups; a thread per head and half of the chunk's
+//    columns): read the head's 64 partial logits from TMEM, push their half into
+//    the peer CTA's shared memory with st.async (asynchronous remote stores that
+//    complete on the peer's mbarrier), add the peer's 64 partials, take the
+//    chunk max over all 64 (both threads of a head compute it identically, so no
+//    synchronisation between them), keep a running max (O is rescaled only when
+//    it grows by more than 2^8), write their half of P = 2^(x - m) as bf16 into
+//    TMEM, where the P·V MMA reads it as its A operand.
 //
 // Decode rows are split over 2 clusters when there are few queries; the second
 // cluster of a row to finish merges the other's partial (O, max, sum) into its own.
@@ -53,18 +56,24 @@ constexpr int kH = 128;        // heads (MMA M)
 constexpr int kD = 576;        // latent + rope
 constexpr int kDC = 512;       // value columns
 constexpr int kNC = 64;        // selected rows per chunk
-constexpr int kNAmax = 5;      // 128-byte column atoms of the larger half
-constexpr int kQBytes = kNAmax * kH * 128;    // 80 KB
-constexpr int kKVStage = kNAmax * kNC * 128;  // 40 KB
-constexpr int kStages = 2;
-constexpr int kXBytes = kH * kNC * 4;         // 32 KB
+constexpr int kQK = kD / 2;    // logit columns per CTA
+constexpr int kKSteps = kQK / 16;
+constexpr int kAtoms = 5;                     // 128-byte column atoms of a gathered row
+constexpr int kKVStage = kAtoms * kNC * 128;  // 40 KB
+constexpr int kStages = 3;
+constexpr int kXBytes = kH * kNC * 4;         // 32 KB: one chunk of the peer's partial logits
 constexpr int kMaxTopK = 2048;
-constexpr int kThreads = 320;                 // producer, MMA, 8 softmax warps
-constexpr int kSmem = kQBytes + kStages * kKVStage + kXBytes + kMaxTopK * 4 + 4096 + 1024;
-constexpr int kTmemCols = 512;                // S0 [0,64) S1 [64,128) O [128,384) P [384,416)
-constexpr int kOCol = 128;
-constexpr int kPCol = 384;                    // P (bf16, 2 per column) for the P·V MMA
+constexpr int kThreads = 352;                 // producer, MMA, 8 softmax warps, producer
+constexpr int kBarBytes = 32 * 8 + 2 * 2 * kH * 4;  // mbarriers and flags, then mx[2][2][128]
+constexpr int kSmem = kStages * kKVStage + 2 * kXBytes + kMaxTopK * 4 + kBarBytes + 1024;
+constexpr int kTmemCols = 512;
+constexpr int kOCol = 0;                      // O: 256 fp32 columns
+constexpr int kQCol = 256;                    // Q: 144 columns (2 bf16 each)
+constexpr int kSCol = 400;                    // S: 64 fp32 columns
+constexpr int kPCol = 464;                    // P: 32 columns (2 bf16 each)
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows > 2^8
+static_assert(kPCol + 32 <= kTmemCols, "TMEM layout");
+static_assert(kStages * kKVStage + 2 * kXBytes >= kH * 256 * 4, "merge staging area");
 
 struct Params {
   Seqs seqs;
@@ -72,6 +81,7 @@ struct Params {
   float scale_log2;  // softmax scale · log2(e)
   int nsplit;
   int out_f32;
+  const __nv_bfloat16* q;
   const int32_t* idx;
   const __nv_bfloat16* kv;
   void* out;
@@ -114,55 +124,56 @@ __device__ __forceinline__ int seq_of_row(const Seqs& s, int t, int lane) {
   return lo;
 }
 
+// The split `sp` of a row with nv selected keys: rows [lo, lo + n) of its list.
+__device__ __forceinline__ void unit_range(int nv, int sp, int nsplit, int& lo, int& n) {
+  lo = (int)((int64_t)nv * sp / nsplit);
+  n = (int)((int64_t)nv * (sp + 1) / nsplit) - lo;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
+sfa_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* qs = smem;
-  uint8_t* kvs = qs + kQBytes;
-  float4* xs = reinterpret_cast<float4*>(kvs + kStages * kKVStage);  // [16][128]: peer's logits
-  int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + kXBytes);
+  uint8_t* kvs = smem;                                                    // [kStages][5][64][128 B]
+  float4* xs = reinterpret_cast<float4*>(kvs + kStages * kKVStage);       // [2][16][128]
+  int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + 2 * kXBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(list + kMaxTopK);
-  uint64_t* kv_full = bars;          // [2]  32 producer lanes (cp.async completion)
-  uint64_t* kv_empty = bars + 2;     // [2]
-  uint64_t* s_full = bars + 4;       // [2]
-  uint64_t* s_empty = bars + 6;      // [2]
-  uint64_t* q_full = bars + 8;
-  uint64_t* q_empty = bars + 9;
-  uint64_t* p_full = bars + 10;
-  uint64_t* p_empty = bars + 11;
-  uint64_t* pv_done = bars + 12;
-  uint64_t* x_full = bars + 13;      // the peer's st.async bytes land here (32 KB per chunk)
-  uint64_t* x_empty = bars + 14;     // the peer's 4 softmax warps: buffer read
-  uint64_t* meta_full = bars + 15;
-  uint64_t* meta_empty = bars + 16;
-  uint64_t* drain = bars + 17;       // [2]: MMA drain, merge copy
-  volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 19);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
-  int* s_last = reinterpret_cast<int*>(bars + 22);
-  uint64_t* sync_a = bars + 23;      // 256 softmax threads: partials written
-  uint64_t* sync_b = bars + 24;      // the arrival count has been taken
-  uint64_t* hsync = bars + 25;       // the 8 softmax warps: per-head halves exchanged
-  float* mx = reinterpret_cast<float*>(bars + 26);  // [2 phases][2 halves][128]
+  uint64_t* kv_full = bars;              // [kStages] 64 producer lanes (cp.async completion)
+  uint64_t* kv_empty = bars + 4;         // [kStages]
+  uint64_t* s_full = bars + 8;
+  uint64_t* s_empty = bars + 9;          // 8 softmax warps have read S
+  uint64_t* q_full = bars + 10;          // 8 softmax warps have stored Q
+  uint64_t* p_full = bars + 11;
+  uint64_t* p_empty = bars + 12;
+  uint64_t* pv_done = bars + 13;
+  uint64_t* x_full = bars + 14;          // [2] the peer's st.async bytes land here
+  uint64_t* x_empty = bars + 16;         // [2] the peer's 8 softmax warps: buffer read
+  uint64_t* meta_full = bars + 18;
+  uint64_t* meta_empty = bars + 19;
+  uint64_t* drain = bars + 20;           // [2]: MMA drain, merge copy
+  uint64_t* sync_a = bars + 22;          // 256 softmax threads: partials written
+  uint64_t* sync_b = bars + 23;          // the arrival count has been taken
+  uint64_t* hsync = bars + 24;           // the 8 softmax warps: per-head halves exchanged
+  volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 25);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 27);
+  int* s_last = reinterpret_cast<int*>(bars + 28);
+  float* mx = reinterpret_cast<float*>(bars + 32);  // [2 phases][2 halves][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int NA = rank ? 5 : 4;                 // column atoms this CTA owns for S
-  const int colbase = rank ? 256 : 0;          // first latent column it owns
+  const int gbase = rank ? 256 : 0;            // first kv column gathered = first output column
   const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   const int nunits = p.seqs.total_q * p.nsplit;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 32); mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 8);
-    }
-    mbar_init(q_full, 1); mbar_init(q_empty, 1);
+    for (int i = 0; i < kStages; ++i) { mbar_init(&kv_full[i], 64); mbar_init(&kv_empty[i], 1); }
+    mbar_init(s_full, 1); mbar_init(s_empty, 8);
+    mbar_init(q_full, 8);
     mbar_init(p_full, 8); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
-    mbar_init(x_full, 1); mbar_init(x_empty, 8);
-    mbar_init(meta_full, 1); mbar_init(meta_empty, 9);
+    for (int i = 0; i < 2; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 8); }
+    mbar_init(meta_full, 1); mbar_init(meta_empty, 10);
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
     mbar_init(sync_a, 256);
@@ -170,7 +181,6 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
     mbar_init(hsync, 8);
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&qmap);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
   tc_fence_before();
@@ -178,118 +188,134 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- producer warp: query block, index compaction, gathers ----------------
-    int gc = 0, qi = 0;
+  if (warp == 0 || warp == 10) {
+    // -------- producer warps: index compaction (warp 0), gathers (32 rows each) --------
+    const int pw = warp == 0 ? 0 : 1;
+    int gc = 0;
     bool stop = false;
     for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
       const int t = u / p.nsplit, sp = u - t * p.nsplit;
-      // the query block needs only t: issue it first
-      if (lane == 0) {
-        if (mbar_wait(q_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
-          mbar_arrive_expect_tx(q_full, NA * kH * 128);
-          for (int a = 0; a < NA; ++a)
-            tma_load_2d(qs + a * (kH * 128), &qmap, q_full, colbase + 64 * a, t * kH);
-        } else {
-          stop = true;
+      int nv;
+      if (pw == 0) {
+        const int b = seq_of_row(p.seqs, t, lane);
+        int q0 = 0, q1 = 0, k0 = 0, k1 = 0;
+        if (lane == 0) {
+          q0 = __ldg(p.seqs.cu_q + b); q1 = __ldg(p.seqs.cu_q + b + 1);
+          k0 = __ldg(p.seqs.cu_k + b); k1 = __ldg(p.seqs.cu_k + b + 1);
         }
-      }
-      qi = ui + 1;
-      if (__shfl_sync(0xffffffffu, stop, 0)) break;
-      // its sequence and position
-      const int b = seq_of_row(p.seqs, t, lane);
-      int q0 = 0, q1 = 0, k0 = 0, k1 = 0;
-      if (lane == 0) {
-        q0 = __ldg(p.seqs.cu_q + b); q1 = __ldg(p.seqs.cu_q + b + 1);
-        k0 = __ldg(p.seqs.cu_k + b); k1 = __ldg(p.seqs.cu_k + b + 1);
-      }
-      q0 = __shfl_sync(0xffffffffu, q0, 0); q1 = __shfl_sync(0xffffffffu, q1, 0);
-      k0 = __shfl_sync(0xffffffffu, k0, 0); k1 = __shfl_sync(0xffffffffu, k1, 0);
-      const int pos = (k1 - k0) - (q1 - q0) + (t - q0);
-      const bool ok = t >= q0 && t < q1 && q1 - q0 <= k1 - k0 && k0 >= 0 &&
-                      k1 <= p.seqs.total_k && k1 - k0 <= p.seqs.max_k_len;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)))
-        break;
-      // valid entries of idx[t, :] in slot order -> list (absolute key rows).  Each lane
-      // owns a contiguous run of up to 64 slots, loaded all at once (independent loads).
-      const int32_t* irow = p.idx + (int64_t)t * p.top_k;
-      const int seg = (p.top_k + 31) / 32;
-      const int s0 = lane * seg;
-      int v[kMaxTopK / 32];
+        q0 = __shfl_sync(0xffffffffu, q0, 0); q1 = __shfl_sync(0xffffffffu, q1, 0);
+        k0 = __shfl_sync(0xffffffffu, k0, 0); k1 = __shfl_sync(0xffffffffu, k1, 0);
+        const int pos = (k1 - k0) - (q1 - q0) + (t - q0);
+        const bool ok = t >= q0 && t < q1 && q1 - q0 <= k1 - k0 && k0 >= 0 &&
+                        k1 <= p.seqs.total_k && k1 - k0 <= p.seqs.max_k_len;
+        // valid entries of idx[t, :] in slot order -> list (absolute key rows).  Each lane
+        // owns a contiguous run of up to 64 slots, loaded all at once (independent loads).
+        const int32_t* irow = p.idx + (int64_t)t * p.top_k;
+        const int seg = (p.top_k + 31) / 32;
+        const int s0 = lane * seg;
+        int v[kMaxTopK / 32];
 #pragma unroll
-      for (int j = 0; j < kMaxTopK / 32; ++j)
-        v[j] = (ok && j < seg && s0 + j < p.top_k) ? __ldg(irow + s0 + j) : -1;
-      int cnt = 0;
-      bool bad = false;
+        for (int j = 0; j < kMaxTopK / 32; ++j)
+          v[j] = (ok && j < seg && s0 + j < p.top_k) ? __ldg(irow + s0 + j) : -1;
+        int cnt = 0;
+        bool bad = false;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK / 32; ++j) {
-        const bool valid = v[j] >= 0 && v[j] <= pos;
-        bad |= !valid && v[j] != -1;
-        cnt += valid;
+        for (int j = 0; j < kMaxTopK / 32; ++j) {
+          const bool valid = v[j] >= 0 && v[j] <= pos;
+          bad |= !valid && v[j] != -1;
+          cnt += valid;
+        }
+        if (bad && sp == 0 && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
+        int before = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, before, o);
+          if (lane >= o) before += y;
+        }
+        nv = __shfl_sync(0xffffffffu, before, 31);
+        before -= cnt;
+        // the previous unit's list is no longer read by either producer
+        if (!__all_sync(0xffffffffu, mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT)))
+          break;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK / 32; ++j)
+          if (v[j] >= 0 && v[j] <= pos) list[before++] = k0 + v[j];
+        __syncwarp();
+        if (lane == 0) { *meta_nv = nv; mbar_arrive(meta_full); }
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(meta_full, ui & 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT)))
+          break;
+        nv = *meta_nv;
       }
-      if (bad && sp == 0 && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
-      int before = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, before, o);
-        if (lane >= o) before += y;
-      }
-      const int nv = __shfl_sync(0xffffffffu, before, 31);
-      before -= cnt;
-#pragma unroll
-      for (int j = 0; j < kMaxTopK / 32; ++j)
-        if (v[j] >= 0 && v[j] <= pos) list[before++] = k0 + v[j];
-      __syncwarp();
-      if (lane == 0) { *meta_nv = nv; mbar_arrive(meta_full); }
-      const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
-      const int n = hi - lo, nch = (n + kNC - 1) / kNC;
-      // gathers: lane = (row sub-index r4 = lane / 8, 16-byte piece j = lane % 8)
+      int lo, n;
+      unit_range(nv, sp, p.nsplit, lo, n);
+      const int nch = (n + kNC - 1) / kNC;
+      // lane = (row sub-index r4 = lane / 8, 16-byte piece lane % 8) for whole atoms;
+      // (r8 = lane / 4, piece lane % 4) for CTA 0's half atom (columns 256..287)
       const int r4 = lane >> 3, jp = lane & 7;
+      const int r8 = lane >> 2, jh = lane & 3;
+      const int natoms = rank ? 5 : 4;
+      const int rbase = 32 * pw;
       for (int c = 0; c < nch; ++c, ++gc) {
-        const int st = gc & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag,
-                                               p.status, DSA_FLAG_TIMEOUT))) { stop = true; break; }
-        int rowid[kNC / 4];
+        const int st = gc % kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((gc / kStages) & 1) ^ 1,
+                                               abort_flag, p.status, DSA_FLAG_TIMEOUT))) {
+          stop = true; break;
+        }
+        int rowid[8];
 #pragma unroll
-        for (int g = 0; g < kNC / 4; ++g) {
-          const int jj = c * kNC + g * 4 + r4;
-          rowid[g] = list[lo + (jj < n ? jj : 0)];
+        for (int g = 0; g < 8; ++g) {
+          const int jj = c * kNC + rbase + g * 4 + r4;
+          rowid[g] = list[lo + (jj < n ? jj : 0)];  // the tail repeats a valid row (masked)
         }
         const uint32_t dst0 = smem_u32(kvs + st * kKVStage);
-        for (int a = 0; a < NA; ++a) {
+        for (int a = 0; a < natoms; ++a) {
 #pragma unroll
-          for (int g = 0; g < kNC / 4; ++g) {
-            const int r = g * 4 + r4;
-            const __nv_bfloat16* src = p.kv + (int64_t)rowid[g] * kD + colbase + a * 64 + jp * 8;
+          for (int g = 0; g < 8; ++g) {
+            const int r = rbase + g * 4 + r4;
+            const __nv_bfloat16* src = p.kv + (int64_t)rowid[g] * kD + gbase + a * 64 + jp * 8;
             cp_async16(dst0 + a * (kNC * 128) + r * 128 + ((jp ^ (r & 7)) * 16), src);
+          }
+        }
+        if (rank == 0) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int r = rbase + g * 8 + r8;
+            const int jj = c * kNC + r;
+            const int row = list[lo + (jj < n ? jj : 0)];
+            const __nv_bfloat16* src = p.kv + (int64_t)row * kD + 256 + jh * 8;
+            cp_async16(dst0 + 4 * (kNC * 128) + r * 128 + ((jh ^ (r & 7)) * 16), src);
           }
         }
         cp_async_arrive_noinc(&kv_full[st]);
       }
+      __syncwarp();
+      if (pw == 1 && lane == 0) mbar_arrive(meta_empty);  // done reading this unit's list
     }
     // every copy issued has landed before the CTA may exit
     cp_async_wait_all();
-    if (lane == 0 && qi > 0) mbar_wait_drain(q_full, (qi - 1) & 1);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(kH, kNC);                  // K-major A and B
       const uint32_t idesc_pv = idesc_bf16(kH, 256, false, true);    // V is MN-major
-      const uint32_t qa = smem_u32(qs), kv0 = smem_u32(kvs);
+      const uint32_t kv0 = smem_u32(kvs);
+      const int koff = rank ? 2 : 0;  // CTA 1's logit columns start half-way into atom 0
       int gc = 0;
       bool stop = false;
       auto pv = [&](int g, int first) -> bool {
         if (!mbar_wait(p_full, g & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) return false;
         tc_fence_after();
-        const uint32_t vb = kv0 + (g & 1) * kKVStage;
+        const uint32_t vb = kv0 + (g % kStages) * kKVStage;
 #pragma unroll
         for (int kk = 0; kk < kNC / 16; ++kk) {  // P from TMEM: 16 rows = 8 columns per step
           const uint64_t bd = sdesc_sw128(vb + kk * 2048, kNC * 128, 1024);
           mma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, bd, idesc_pv,
                       (first == 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kv_empty[g & 1]);
+        mma_commit(&kv_empty[g % kStages]);
         mma_commit(p_empty);
         mma_commit(pv_done);
         return true;
@@ -298,32 +324,31 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
         if (!mbar_wait(meta_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         const int nv = *meta_nv;
         mbar_arrive(meta_empty);
-        const int t = u / p.nsplit, sp = u - t * p.nsplit;
-        (void)t;
-        const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
-        const int nch = (hi - lo + kNC - 1) / kNC;
+        const int sp = u % p.nsplit;
+        int lo, n;
+        unit_range(nv, sp, p.nsplit, lo, n);
+        const int nch = (n + kNC - 1) / kNC;
         if (!mbar_wait(q_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         tc_fence_after();
-        if (nch == 0) { mma_commit(q_empty); continue; }
+        if (nch == 0) continue;
         const int g_first = gc;
         for (int c = 0; c < nch; ++c, ++gc) {
-          const int st = gc & 1;
-          if (!mbar_wait(&kv_full[st], (gc >> 1) & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT) ||
-              !mbar_wait(&s_empty[st], ((gc >> 1) & 1) ^ 1, abort_flag, p.status,
-                         DSA_FLAG_TIMEOUT)) { stop = true; break; }
+          const int st = gc % kStages;
+          if (!mbar_wait(&kv_full[st], (gc / kStages) & 1, abort_flag, p.status,
+                         DSA_FLAG_TIMEOUT) ||
+              !mbar_wait(s_empty, (gc & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
+            stop = true; break;
+          }
           fence_proxy_async_smem();  // the cp.async writes, seen by the tensor core
           tc_fence_after();
           const uint32_t kb = kv0 + st * kKVStage;
-          for (int a = 0; a < NA; ++a) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(qa + a * (kH * 128) + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kb + a * (kNC * 128) + kk * 32, 16, 1024);
-              mma_bf16(tmem + st * kNC, ad, bd, idesc_s, (a | kk) ? 1u : 0u);
-            }
+          for (int i = 0; i < kKSteps; ++i) {
+            const int g = i + koff;
+            const uint64_t bd = sdesc_sw128(kb + (g >> 2) * (kNC * 128) + (g & 3) * 32, 16, 1024);
+            mma_bf16_ts(tmem + kSCol, tmem + kQCol + i * 8, bd, idesc_s, i ? 1u : 0u);
           }
-          mma_commit(&s_full[st]);
-          if (c == nch - 1) mma_commit(q_empty);
+          mma_commit(s_full);
           if (c > 0 && !pv(gc - 1, gc - 1 == g_first)) { stop = true; break; }
         }
         if (stop) break;
@@ -357,67 +382,102 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
       return slot[(1 - half) * 128 + h];
     };
     for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
+      const int t = u / p.nsplit, sp = u - t * p.nsplit;
+      // this thread's 72 query columns (144 bf16) -> TMEM, the logit MMA's A operand.
+      // The previous unit's logit MMAs are complete: this thread has read all their S.
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + ((int64_t)t * kH + h) * kD + (rank ? kQK : 0) + 144 * half);
+        uint4 qv[18];
+#pragma unroll
+        for (int i = 0; i < 18; ++i) qv[i] = __ldg(src + i);
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          w[4 * i] = qv[i].x; w[4 * i + 1] = qv[i].y; w[4 * i + 2] = qv[i].z; w[4 * i + 3] = qv[i].w;
+        }
+        tmem_st32(lane_base + kQCol + 72 * half, w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          w[4 * i] = qv[8 + i].x; w[4 * i + 1] = qv[8 + i].y;
+          w[4 * i + 2] = qv[8 + i].z; w[4 * i + 3] = qv[8 + i].w;
+        }
+        tmem_st32(lane_base + kQCol + 72 * half + 32, w);
+        const uint32_t w8[8] = {qv[16].x, qv[16].y, qv[16].z, qv[16].w,
+                                qv[17].x, qv[17].y, qv[17].z, qv[17].w};
+        tmem_st8(lane_base + kQCol + 72 * half + 64, w8);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(meta_full, ui & 1, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT))) break;
       const int nv = *meta_nv;
       __syncwarp();
       if (lane == 0) mbar_arrive(meta_empty);
-      const int t = u / p.nsplit, sp = u - t * p.nsplit;
-      const int lo = (int)((int64_t)nv * sp / p.nsplit), hi = (int)((int64_t)nv * (sp + 1) / p.nsplit);
-      const int n = hi - lo, nch = (n + kNC - 1) / kNC;
+      int lo, n;
+      unit_range(nv, sp, p.nsplit, lo, n);
+      const int nch = (n + kNC - 1) / kNC;
       float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the sum
       for (int c = 0; c < nch; ++c, ++gc) {
-        const int sb = gc & 1;
         const int rows_in = min(kNC, n - c * kNC);
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (gc >> 1) & 1, abort_flag, p.status,
+        const int xb = gc & 1;               // exchange buffer
+        const uint32_t xph = (gc >> 1) & 1;  // parity of its use count
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full, gc & 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) { stop = true; break; }
         tc_fence_after();
-        float s[32];
+        float s[64];
         {
           uint32_t r[32];
-          tmem_ld32(lane_base + sb * kNC + 32 * half, r);
+          tmem_ld32(lane_base + kSCol, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+          tmem_ld32(lane_base + kSCol + 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[sb]);
-        // exchange the partial logits: st.async ours into the peer's buffer ([16][128]
-        // float4; the bytes complete on the peer's x_full), read the peer's from ours
-        if (leader) mbar_arrive_expect_tx(x_full, kXBytes);
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_empty, (gc & 1) ^ 1, abort_flag,
+        if (lane == 0) mbar_arrive(s_empty);
+        // push our half of the partial logits into the peer's buffer ([16][128] float4;
+        // the bytes complete on the peer's x_full), then read the peer's 64 from ours
+        if (leader) mbar_arrive_expect_tx(&x_full[xb], kXBytes);
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&x_empty[xb], xph ^ 1, abort_flag,
                                                        p.status, DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
+        const uint32_t xdst = xs_peer + (uint32_t)(xb * kXBytes);
+        const uint32_t xbar = x_full_peer + (uint32_t)(xb * 8);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_async_f4(xs_peer + (uint32_t)(((8 * half + q) * kH + h) * 16),
-                      make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]), x_full_peer);
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(x_full, gc & 1, abort_flag, p.status,
+        for (int q = 0; q < 8; ++q) {
+          const float a0 = half ? s[32 + 4 * q] : s[4 * q];
+          const float a1 = half ? s[33 + 4 * q] : s[4 * q + 1];
+          const float a2 = half ? s[34 + 4 * q] : s[4 * q + 2];
+          const float a3 = half ? s[35 + 4 * q] : s[4 * q + 3];
+          st_async_f4(xdst + (uint32_t)(((8 * half + q) * kH + h) * 16),
+                      make_float4(a0, a1, a2, a3), xbar);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&x_full[xb], xph, abort_flag, p.status,
                                                        DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
-        float4 xo[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) xo[q] = xs[(8 * half + q) * kH + h];
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(x_empty_peer);  // our buffer may be refilled
+        const float4* xin = xs + xb * (kXBytes / 16);
         float m_c = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float other[4] = {xo[q].x, xo[q].y, xo[q].z, xo[q].w};
+        for (int q = 0; q < 16; ++q) {
+          const float4 x4 = xin[q * kH + h];
+          const float other[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * q + e;
-            const float lo_part = rank ? other[e] : s[i];
-            const float hi_part = rank ? s[i] : other[e];
-            const float x = (lo_part + hi_part) * p.scale_log2;
-            s[i] = 32 * half + i < rows_in ? x : -INFINITY;
+            const float x = (s[i] + other[e]) * p.scale_log2;  // a + b == b + a exactly
+            s[i] = i < rows_in ? x : -INFINITY;
             m_c = fmaxf(m_c, s[i]);
           }
         }
-        m_c = fmaxf(m_c, exchange(m_c));
-        if (stop) break;
+        __syncwarp();
+        // the reads above fed m_c: the buffer may be refilled
+        if (lane == 0) mbar_arrive_remote_relaxed(x_empty_peer + (uint32_t)(xb * 8));
         // running max: move the reference only when it grows by more than 2^8
         const bool grow = m_c > m_ref + kRescaleLog2;
         const float m_new = grow ? m_c : m_ref;
@@ -441,8 +501,9 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(s[2 * i] - m_ref),
-                                                          ex2(s[2 * i + 1] - m_ref));
+          const float x0 = half ? s[32 + 2 * i] : s[2 * i];
+          const float x1 = half ? s[33 + 2 * i] : s[2 * i + 1];
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(x0 - m_ref), ex2(x1 - m_ref));
           const float2 f2 = __bfloat1622float2(b2);
           l += f2.x + f2.y;
           pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
@@ -471,7 +532,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
       if (p.nsplit == 1) {
         const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
         uint8_t* orow = static_cast<uint8_t*>(p.out) +
-                        (((int64_t)t * kH + h) * kDC + colbase + ocol) * (p.out_f32 ? 4 : 2);
+                        (((int64_t)t * kH + h) * kDC + gbase + ocol) * (p.out_f32 ? 4 : 2);
         for (int b = 0; b < 4; ++b) {
           uint32_t r[32];
           if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
@@ -537,7 +598,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
           // 128 KB into the (now idle) query/KV area, then each thread merges.
           __threadfence();
           const int64_t other = ((int64_t)t * p.nsplit + (1 - sp)) * 2 + rank;
-          float4* po2 = reinterpret_cast<float4*>(qs);
+          float4* po2 = reinterpret_cast<float4*>(kvs);  // idle ring + exchange area
           if (leader) {
             fence_proxy_async_all();
             mbar_arrive_expect_tx(drain + 1, kH * 256 * 4);
@@ -559,7 +620,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
           if (!__all_sync(0xffffffffu, mbar_wait(drain + 1, 0, abort_flag, p.status,
                                                  DSA_FLAG_TIMEOUT))) break;
           uint8_t* orow = static_cast<uint8_t*>(p.out) +
-                          (((int64_t)t * kH + h) * kDC + colbase + ocol) * (p.out_f32 ? 4 : 2);
+                          (((int64_t)t * kH + h) * kDC + gbase + ocol) * (p.out_f32 ? 4 : 2);
           for (int b = 0; b < 4; ++b) {
             uint32_t r[32];
             if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
@@ -617,10 +678,13 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, Params p) {
 
 bool sfa_tc_eligible(const SfaArgs& a) {
   return a.kv_dtype == DSA_BF16 && a.h == kH && a.d_c == kDC && a.d_rope == kD - kDC &&
-         a.top_k <= kMaxTopK;
+         a.top_k <= kMaxTopK && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(a.kv) & 15) == 0;
 }
 
-// Split each row over 2 clusters when that still leaves every cluster one unit.
+// Split each row over 2 clusters when that still leaves every cluster one unit.  With a
+// split, units = 2 * total_q <= num_sms / 2 = clusters, so a cluster never runs a second
+// unit: the merge may stage the partner's partial in the idle ring and exchange buffers.
 int sfa_tc_nsplit(int total_q) { return total_q > 0 && num_sms() >= 4 * total_q ? 2 : 1; }
 
 size_t sfa_tc_scratch_bytes(int total_q) {
@@ -634,16 +698,13 @@ size_t sfa_tc_scratch_bytes(int total_q) {
 int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
   const int ns = sfa_tc_nsplit(a.seqs.total_q);
-  CUtensorMap qmap;
-  int rc = make_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD,
-                        (uint64_t)a.seqs.total_q * kH, kD * 2, 64, kH);
-  if (rc != DSA_OK) return rc;
   Params p{};
   p.seqs = a.seqs;
   p.top_k = a.top_k;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.nsplit = ns;
   p.out_f32 = a.out_dtype == DSA_F32;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.idx = a.idx;
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
   p.out = a.out;
@@ -667,7 +728,7 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   const int max_clusters = num_sms() / 2;
   const int clusters = (int)(units < max_clusters ? units : max_clusters);
   DSA_LAUNCH("sfa_tc", stream,
-             sfa_tc_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(qmap, p));
+             sfa_tc_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(p));
   return check_launch("sfa_tc");
 }
 
