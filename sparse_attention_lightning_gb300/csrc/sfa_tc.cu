@@ -15,9 +15,10 @@
 // bf16 = 144 KB) and a 128 x 512 fp32 output accumulator, which is all 512 TMEM
 // columns with no room for the logits.  So a 2-CTA cluster splits the work:
 //  * logits: CTA 0 takes columns 0..287, CTA 1 columns 288..575 (18 K-steps
-//    each); each computes a partial S over its columns and the two partial S
-//    tiles are added through distributed shared memory, in the same order in both
-//    CTAs, so both hold identical logits and take identical softmax decisions;
+//    each); each computes a partial S over its columns and sends it to the other
+//    through distributed shared memory (scaled to log2 units, as fp16); each CTA
+//    adds the peer's partial to its own fp32 one and runs its own online softmax
+//    (max, sum, O) over the full logits, so the CTAs share nothing else;
 //  * values: CTA 0 accumulates output columns 0..255, CTA 1 columns 256..511.
 // So CTA 0 gathers columns 0..287 of every selected row and CTA 1 columns
 // 256..575.  The CTA's 288 query columns live in TMEM (the logit MMA reads its A
@@ -44,6 +45,8 @@
 // Decode rows are split over 2 clusters when there are few queries; the second
 // cluster of a row to finish merges the other's partial (O, max, sum) into its own.
 // Every wait is bounded (DSA_FLAG_TIMEOUT).
+#include <cuda_fp16.h>
+
 #include "dsa_internal.cuh"
 #include "tc_sm100.cuh"
 
@@ -61,7 +64,7 @@ constexpr int kKSteps = kQK / 16;
 constexpr int kAtoms = 5;                     // 128-byte column atoms of a gathered row
 constexpr int kKVStage = kAtoms * kNC * 128;  // 40 KB
 constexpr int kStages = 3;
-constexpr int kXBytes = kH * kNC * 4;         // 32 KB: one chunk of the peer's partial logits
+constexpr int kXBytes = kH * kNC * 2;         // 16 KB: one chunk of the peer's partial logits (fp16)
 constexpr int kMaxTopK = 2048;
 constexpr int kThreads = 352;                 // producer, MMA, 8 softmax warps, producer
 constexpr int kBarBytes = 32 * 8 + 2 * 2 * kH * 4;  // mbarriers and flags, then mx[2][2][128]
@@ -135,7 +138,7 @@ sfa_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* kvs = smem;                                                    // [kStages][5][64][128 B]
-  float4* xs = reinterpret_cast<float4*>(kvs + kStages * kKVStage);       // [2][16][128]
+  uint4* xs = reinterpret_cast<uint4*>(kvs + kStages * kKVStage);         // [2][8][128] x 8 fp16
   int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + 2 * kXBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(list + kMaxTopK);
   uint64_t* kv_full = bars;              // [kStages] 64 producer lanes (cp.async completion)
@@ -439,40 +442,54 @@ sfa_tc_kernel(Params p) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_empty);
-        // push our half of the partial logits into the peer's buffer ([16][128] float4;
-        // the bytes complete on the peer's x_full), then read the peer's 64 from ours
+        // push our half of the partial logits, scaled to log2 units and rounded to fp16, into
+        // the peer's buffer ([8][128] x 8 halves; the bytes complete on the peer's x_full),
+        // then read the peer's 64 from ours.  The link between the two SMs moves ~12 B per
+        // clock, so the exchange is half the time it would be in fp32; fp16 keeps 2^-11
+        // relative precision, below the bf16 rounding that P gets anyway.
         if (leader) mbar_arrive_expect_tx(&x_full[xb], kXBytes);
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&x_empty[xb], xph ^ 1, abort_flag,
-                                                       p.status, DSA_FLAG_TIMEOUT))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xph ^ 1, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
         const uint32_t xdst = xs_peer + (uint32_t)(xb * kXBytes);
         const uint32_t xbar = x_full_peer + (uint32_t)(xb * 8);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float a0 = half ? s[32 + 4 * q] : s[4 * q];
-          const float a1 = half ? s[33 + 4 * q] : s[4 * q + 1];
-          const float a2 = half ? s[34 + 4 * q] : s[4 * q + 2];
-          const float a3 = half ? s[35 + 4 * q] : s[4 * q + 3];
-          st_async_f4(xdst + (uint32_t)(((8 * half + q) * kH + h) * 16),
-                      make_float4(a0, a1, a2, a3), xbar);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&x_full[xb], xph, abort_flag, p.status,
-                                                       DSA_FLAG_TIMEOUT))) {
-          stop = true; break;
-        }
-        const float4* xin = xs + xb * (kXBytes / 16);
-        float m_c = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 x4 = xin[q * kH + h];
-          const float other[4] = {x4.x, x4.y, x4.z, x4.w};
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int i = 4 * q + e;
-            const float x = (s[i] + other[e]) * p.scale_log2;  // a + b == b + a exactly
-            s[i] = i < rows_in ? x : -INFINITY;
-            m_c = fmaxf(m_c, s[i]);
+            const int i0 = 8 * q + 2 * e;
+            const float a = (half ? s[32 + i0] : s[i0]) * p.scale_log2;
+            const float b = (half ? s[33 + i0] : s[i0 + 1]) * p.scale_log2;
+            const __half2 h2 = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f),
+                                                 fminf(fmaxf(b, -65504.f), 65504.f));
+            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          st_async_u4(xdst + (uint32_t)(((4 * half + q) * kH + h) * 16),
+                      make_uint4(w[0], w[1], w[2], w[3]), xbar);
+        }
+        // CTA-scope wait: the peer's st.async bytes complete on this CTA's own mbarrier (as a
+        // TMA write would), and polling with cluster-scope acquire stalls the tensor core
+        if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xb], xph, abort_flag, p.status,
+                                               DSA_FLAG_TIMEOUT))) {
+          stop = true; break;
+        }
+        const uint4* xin = xs + xb * (kXBytes / 16);
+        float m_c = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 x4 = xin[q * kH + h];
+          const uint32_t wv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 o2 = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+            const int i = 8 * q + 2 * e;
+            const float x0 = fmaf(s[i], p.scale_log2, o2.x);
+            const float x1 = fmaf(s[i + 1], p.scale_log2, o2.y);
+            s[i] = i < rows_in ? x0 : -INFINITY;
+            s[i + 1] = i + 1 < rows_in ? x1 : -INFINITY;
+            m_c = fmaxf(m_c, fmaxf(s[i], s[i + 1]));
           }
         }
         __syncwarp();

@@ -392,6 +392,14 @@ __device__ __forceinline__ void st_async_f4(uint32_t cluster_addr, float4 v, uin
       : "memory");
 }
 
+__device__ __forceinline__ void st_async_u4(uint32_t cluster_addr, uint4 v, uint32_t cluster_mbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_mbar)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
                "f"(v.y), "f"(v.z), "f"(v.w)
