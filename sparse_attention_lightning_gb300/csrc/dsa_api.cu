@@ -213,7 +213,7 @@ size_t segcnt_bytes(const dsa_problem* p) {
   return use_topk_hist(p) ? (size_t)p->total_q * topk_seg_segments(p->max_k_len) * 8 : 0;
 }
 
-// SFA scratch (split-row partials of the tensor-core path; 0 bytes otherwise).
+// SFA scratch of the tensor-core path (per-CTA key-row lists, split-row partials).
 size_t sfa_scratch_bytes(const dsa_problem* p) {
   const bool tc = p->kv_dtype == DSA_BF16 && p->h == 128 && p->d_c == 512 && p->d_rope == 64;
   return tc ? sfa_tc_scratch_bytes(p->total_q) : 0;

@@ -16,15 +16,16 @@
 // columns with no room for the logits.  So a 2-CTA cluster splits the work:
 //  * logits: CTA 0 takes columns 0..287, CTA 1 columns 288..575 (18 K-steps
 //    each); each computes a partial S over its columns and sends it to the other
-//    through distributed shared memory (scaled to log2 units, as fp16); each CTA
-//    adds the peer's partial to its own fp32 one and runs its own online softmax
-//    (max, sum, O) over the full logits, so the CTAs share nothing else;
+//    through distributed shared memory (in log2 units, as fp16); both CTAs add the
+//    same two fp16 partials, so they hold identical logits and take identical
+//    softmax decisions;
 //  * values: CTA 0 accumulates output columns 0..255, CTA 1 columns 256..511.
 // So CTA 0 gathers columns 0..287 of every selected row and CTA 1 columns
 // 256..575.  The CTA's 288 query columns live in TMEM (the logit MMA reads its A
-// operand from there), which leaves shared memory to a 3-stage ring of gathered
-// rows and a double exchange buffer.  TMEM: O (128 x 256 fp32) | Q (144 columns
-// of bf16 pairs) | S (128 x 64 fp32) | P (64 bf16 per head).
+// operand from there), which leaves shared memory to a 4-stage ring of gathered
+// rows and double send and receive exchange buffers.  TMEM: O (128 x 256 fp32) |
+// Q (144 columns of bf16 pairs) | S (128 x 64 fp32) | P (64 bf16 per head) | 8
+// columns for swapping per-head values between the two halves.
 //
 // Per chunk of 64 selected rows:
 //  * two producer warps (32 rows each): the 16-byte pieces of the CTA's columns
@@ -34,12 +35,14 @@
 //    K-major in shared memory), then, once P is ready, O += P · V (M=128, N=256,
 //    K=64; P from TMEM, V read MN-major straight from the gathered tile);
 //  * softmax warps (two warpgroups; a thread per head and half of the chunk's
-//    columns): read the head's 64 partial logits from TMEM, push their half into
-//    the peer CTA's shared memory with st.async (asynchronous remote stores that
-//    complete on the peer's mbarrier), add the peer's 64 partials, take the
-//    chunk max over all 64 (both threads of a head compute it identically, so no
-//    synchronisation between them), keep a running max (O is rescaled only when
-//    it grows by more than 2^8), write their half of P = 2^(x - m) as bf16 into
+//    columns): read their 32 partial logits from TMEM (S is then free for the next
+//    chunk's MMA), scale them to log2 units, round to fp16 and stage them; the last
+//    warp to stage ships the CTA's 16 KB to the peer with one bulk copy.  A chunk is
+//    staged before the previous one is processed whenever its logits are ready, so
+//    the exchange overlaps the softmax.  Processing adds the peer's fp16 partials to
+//    the thread's own (the same sum in both CTAs), takes the chunk max (the two halves
+//    of a head swap theirs through TMEM), keeps a running max (O is rescaled only when
+//    it grows by more than 2^8) and writes its half of P = 2^(x - m) as bf16 into
 //    TMEM, where the P·V MMA reads it as its A operand.
 //
 // Decode rows are split over 2 clusters when there are few queries; the second
@@ -63,19 +66,21 @@ constexpr int kQK = kD / 2;    // logit columns per CTA
 constexpr int kKSteps = kQK / 16;
 constexpr int kAtoms = 5;                     // 128-byte column atoms of a gathered row
 constexpr int kKVStage = kAtoms * kNC * 128;  // 40 KB
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kXBytes = kH * kNC * 2;         // 16 KB: one chunk of the peer's partial logits (fp16)
 constexpr int kMaxTopK = 2048;
 constexpr int kThreads = 352;                 // producer, MMA, 8 softmax warps, producer
-constexpr int kBarBytes = 32 * 8 + 2 * 2 * kH * 4;  // mbarriers and flags, then mx[2][2][128]
-constexpr int kSmem = kStages * kKVStage + 2 * kXBytes + kMaxTopK * 4 + kBarBytes + 1024;
+constexpr int kBarBytes = 48 * 8;             // mbarriers and flags
+constexpr int kSmem = kStages * kKVStage + 4 * kXBytes + kBarBytes + 1024;
 constexpr int kTmemCols = 512;
 constexpr int kOCol = 0;                      // O: 256 fp32 columns
 constexpr int kQCol = 256;                    // Q: 144 columns (2 bf16 each)
 constexpr int kSCol = 400;                    // S: 64 fp32 columns
 constexpr int kPCol = 464;                    // P: 32 columns (2 bf16 each)
+constexpr int kXCol = 496;                    // 4 columns: the two halves' sums, 2 phases
+constexpr int kMCol = 500;                    // 4 columns: the two halves' chunk maxima, 2 phases
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows > 2^8
-static_assert(kPCol + 32 <= kTmemCols, "TMEM layout");
+static_assert(kMCol + 4 <= kTmemCols, "TMEM layout");
 static_assert(kStages * kKVStage + 2 * kXBytes >= kH * 256 * 4, "merge staging area");
 
 struct Params {
@@ -92,6 +97,7 @@ struct Params {
   float4* part_o;    // [total_q * nsplit * 2][64][128] float4 (nsplit > 1)
   float* part_ml;    // [total_q * nsplit * 2][128][2]
   int* counters;     // [total_q * 2], zero at launch
+  int32_t* lists;    // [gridDim.x][kMaxTopK]: each CTA's compacted key rows of its unit
   uint32_t* status;
 };
 
@@ -139,8 +145,9 @@ sfa_tc_kernel(Params p) {
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* kvs = smem;                                                    // [kStages][5][64][128 B]
   uint4* xs = reinterpret_cast<uint4*>(kvs + kStages * kKVStage);         // [2][8][128] x 8 fp16
-  int32_t* list = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(xs) + 2 * kXBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(list + kMaxTopK);
+  uint4* xsend = xs + 2 * (kXBytes / 16);                                  // [2][8][128]: ours, staged
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xsend + 2 * (kXBytes / 16));
+  int32_t* list = p.lists + (int64_t)blockIdx.x * kMaxTopK;  // global: written and read here
   uint64_t* kv_full = bars;              // [kStages] 64 producer lanes (cp.async completion)
   uint64_t* kv_empty = bars + 4;         // [kStages]
   uint64_t* s_full = bars + 8;
@@ -161,7 +168,8 @@ sfa_tc_kernel(Params p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 27);
   int* s_last = reinterpret_cast<int*>(bars + 28);
-  float* mx = reinterpret_cast<float*>(bars + 32);  // [2 phases][2 halves][128]
+  uint64_t* pairb = bars + 29;           // [4] the two softmax warps of a lane quarter
+  uint32_t* x_count = reinterpret_cast<uint32_t*>(bars + 33);  // [2] staging arrivals, ever
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -175,7 +183,11 @@ sfa_tc_kernel(Params p) {
     mbar_init(s_full, 1); mbar_init(s_empty, 8);
     mbar_init(q_full, 8);
     mbar_init(p_full, 8); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
-    for (int i = 0; i < 2; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 8); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 8);
+      x_count[i] = 0;
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&pairb[i], 2);
     mbar_init(meta_full, 1); mbar_init(meta_empty, 10);
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
@@ -261,24 +273,40 @@ sfa_tc_kernel(Params p) {
       const int r8 = lane >> 2, jh = lane & 3;
       const int natoms = rank ? 5 : 4;
       const int rbase = 32 * pw;
+      // this warp's key rows of chunk c (the tail repeats a valid row, masked later): loaded
+      // a chunk ahead, so their latency hides behind the previous chunk's copies
+      int rowid[8], rowh[4];
+      auto load_rows = [&](int c) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int jj = c * kNC + rbase + g * 4 + r4;
+          rowid[g] = list[lo + (jj < n ? jj : 0)];
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int jj = c * kNC + rbase + g * 8 + r8;
+          rowh[g] = list[lo + (jj < n ? jj : 0)];
+        }
+      };
+      if (nch > 0) load_rows(0);
       for (int c = 0; c < nch; ++c, ++gc) {
         const int st = gc % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((gc / kStages) & 1) ^ 1,
                                                abort_flag, p.status, DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
-        int rowid[8];
+        int cur[8], curh[4];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int jj = c * kNC + rbase + g * 4 + r4;
-          rowid[g] = list[lo + (jj < n ? jj : 0)];  // the tail repeats a valid row (masked)
-        }
+        for (int g = 0; g < 8; ++g) cur[g] = rowid[g];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) curh[g] = rowh[g];
+        if (c + 1 < nch) load_rows(c + 1);
         const uint32_t dst0 = smem_u32(kvs + st * kKVStage);
         for (int a = 0; a < natoms; ++a) {
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             const int r = rbase + g * 4 + r4;
-            const __nv_bfloat16* src = p.kv + (int64_t)rowid[g] * kD + gbase + a * 64 + jp * 8;
+            const __nv_bfloat16* src = p.kv + (int64_t)cur[g] * kD + gbase + a * 64 + jp * 8;
             cp_async16(dst0 + a * (kNC * 128) + r * 128 + ((jp ^ (r & 7)) * 16), src);
           }
         }
@@ -286,9 +314,7 @@ sfa_tc_kernel(Params p) {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const int r = rbase + g * 8 + r8;
-            const int jj = c * kNC + r;
-            const int row = list[lo + (jj < n ? jj : 0)];
-            const __nv_bfloat16* src = p.kv + (int64_t)row * kD + 256 + jh * 8;
+            const __nv_bfloat16* src = p.kv + (int64_t)curh[g] * kD + 256 + jh * 8;
             cp_async16(dst0 + 4 * (kNC * 128) + r * 128 + ((jh ^ (r & 7)) * 16), src);
           }
         }
@@ -308,21 +334,6 @@ sfa_tc_kernel(Params p) {
       const int koff = rank ? 2 : 0;  // CTA 1's logit columns start half-way into atom 0
       int gc = 0;
       bool stop = false;
-      auto pv = [&](int g, int first) -> bool {
-        if (!mbar_wait(p_full, g & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) return false;
-        tc_fence_after();
-        const uint32_t vb = kv0 + (g % kStages) * kKVStage;
-#pragma unroll
-        for (int kk = 0; kk < kNC / 16; ++kk) {  // P from TMEM: 16 rows = 8 columns per step
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kNC * 128, 1024);
-          mma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, bd, idesc_pv,
-                      (first == 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&kv_empty[g % kStages]);
-        mma_commit(p_empty);
-        mma_commit(pv_done);
-        return true;
-      };
       for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
         if (!mbar_wait(meta_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         const int nv = *meta_nv;
@@ -334,28 +345,66 @@ sfa_tc_kernel(Params p) {
         if (!mbar_wait(q_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         tc_fence_after();
         if (nch == 0) continue;
-        const int g_first = gc;
-        for (int c = 0; c < nch; ++c, ++gc) {
-          const int st = gc % kStages;
-          if (!mbar_wait(&kv_full[st], (gc / kStages) & 1, abort_flag, p.status,
-                         DSA_FLAG_TIMEOUT) ||
-              !mbar_wait(s_empty, (gc & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) {
-            stop = true; break;
-          }
-          fence_proxy_async_smem();  // the cp.async writes, seen by the tensor core
-          tc_fence_after();
-          const uint32_t kb = kv0 + st * kKVStage;
+        // The softmax warps release S(c) early (they stage it and move on) and hand back P(c)
+        // late, so the logit MMA of a chunk may go ahead of the P·V of an earlier one: issue
+        // whichever has its inputs ready (bounded polling).
+        const int g0 = gc;
+        int si = 0, pi = 0;
+        uint32_t spins = 0;
+        uint64_t t0 = 0;
+        while (pi < nch) {
+          bool did = false;
+          if (si < nch) {
+            const int g = g0 + si, st = g % kStages;
+            if (mbar_test(smem_u32(&kv_full[st]), (g / kStages) & 1) &&
+                mbar_test(smem_u32(s_empty), (g & 1) ^ 1)) {
+              fence_proxy_async_smem();  // the cp.async writes, seen by the tensor core
+              tc_fence_after();
+              // descriptor of the stage's first K-step; later K-steps add their byte offset / 16
+              // to its start-address field
+              const uint64_t bd0 = sdesc_sw128(kv0 + st * kKVStage, 16, 1024);
 #pragma unroll
-          for (int i = 0; i < kKSteps; ++i) {
-            const int g = i + koff;
-            const uint64_t bd = sdesc_sw128(kb + (g >> 2) * (kNC * 128) + (g & 3) * 32, 16, 1024);
-            mma_bf16_ts(tmem + kSCol, tmem + kQCol + i * 8, bd, idesc_s, i ? 1u : 0u);
+              for (int i = 0; i < kKSteps; ++i) {
+                const int k = i + koff;
+                const uint64_t bd = bd0 + (uint64_t)(((k >> 2) * (kNC * 128) + (k & 3) * 32) >> 4);
+                mma_bf16_ts(tmem + kSCol, tmem + kQCol + i * 8, bd, idesc_s, i ? 1u : 0u);
+              }
+              mma_commit(s_full);
+              ++si;
+              did = true;
+            }
           }
-          mma_commit(s_full);
-          if (c > 0 && !pv(gc - 1, gc - 1 == g_first)) { stop = true; break; }
+          if (pi < si) {
+            const int g = g0 + pi;
+            if (mbar_test(smem_u32(p_full), g & 1)) {
+              tc_fence_after();
+              const uint32_t vb = kv0 + (g % kStages) * kKVStage;
+#pragma unroll
+              for (int kk = 0; kk < kNC / 16; ++kk) {  // P from TMEM: 16 rows = 8 columns a step
+                const uint64_t bd = sdesc_sw128(vb + kk * 2048, kNC * 128, 1024);
+                mma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, bd, idesc_pv,
+                            (pi > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&kv_empty[g % kStages]);
+              mma_commit(p_empty);
+              mma_commit(pv_done);
+              ++pi;
+              did = true;
+            }
+          }
+          if (did) { spins = 0; continue; }
+          if (spins++ == 0) t0 = globaltimer_ns();
+          if ((spins & 15u) == 0) {
+            if (*abort_flag) { stop = true; break; }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(p.status, DSA_FLAG_TIMEOUT);
+              stop = true;
+              break;
+            }
+          }
         }
-        if (stop) break;
-        if (!pv(gc - 1, gc - 1 == g_first)) break;
+        gc = g0 + nch;
       }
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
@@ -372,17 +421,84 @@ sfa_tc_kernel(Params p) {
     const bool leader = threadIdx.x == 64;
     int gc = 0, nsync = 0;
     bool stop = false;
-    // combine a per-head value with the other half's (bounded 8-warp exchange)
+    // Stage chunk g: read this thread's 32 partial logits from TMEM (then S is free for
+    // the next logit MMA), scale them to log2 units, round to fp16 and write them to the
+    // staging buffer ([8][128] x 8 halves: both halves of every head).  The last of the 8
+    // warps to stage ships the 16 KB to the peer with one bulk copy that completes on the
+    // peer's x_full.  The link between the two SMs moves ~12 B per clock: fp16 halves the
+    // time fp32 would take and keeps 2^-11 relative precision, below the bf16 rounding P
+    // gets anyway; one bulk copy (rather than per-thread remote stores, which update the
+    // peer's mbarrier every 16 bytes) leaves the peer's tensor core undisturbed.
+    auto stage = [&](int g, uint32_t (&own)[16]) -> bool {
+      const int xb = g & 1;
+      const uint32_t xph = (g >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort_flag, p.status,
+                                             DSA_FLAG_TIMEOUT))) return false;
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(lane_base + kSCol + 32 * half, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      // our x_full will take this chunk's bytes from the peer
+      if (leader) mbar_arrive_expect_tx(&x_full[xb], kXBytes);
+      // the peer has read what we sent two chunks ago, so our copy of it is complete
+      if (!__all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xph ^ 1, abort_flag, p.status,
+                                             DSA_FLAG_TIMEOUT))) return false;
+      uint4* xout = xsend + xb * (kXBytes / 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = __uint_as_float(r[8 * q + 2 * e]) * p.scale_log2;
+          const float b = __uint_as_float(r[8 * q + 2 * e + 1]) * p.scale_log2;
+          const __half2 h2 = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f),
+                                               fminf(fmaxf(b, -65504.f), 65504.f));
+          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          own[4 * q + e] = w[e];
+        }
+        xout[(4 * half + q) * kH + h] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();  // our generic writes, seen by the bulk copy
+      __syncwarp();
+      if (lane == 0) {
+        uint32_t before;
+        asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                     : "=r"(before) : "r"(smem_u32(&x_count[xb])) : "memory");
+        if ((before & 7u) == 7u)
+          bulk_s2peer(xs_peer + (uint32_t)(xb * kXBytes), xout, kXBytes,
+                      x_full_peer + (uint32_t)(xb * 8));
+      }
+      return true;
+    };
+    // the other half's chunk maximum of head h (the warp pair of this lane quarter)
+    auto pair_max = [&](float v, int g) -> float {
+      const uint32_t col = lane_base + kMCol + 2 * (g & 1);
+      tmem_st1(col + half, __float_as_uint(v));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pairb[quarter]);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&pairb[quarter], g & 1, abort_flag,
+                                                        p.status, DSA_FLAG_TIMEOUT));
+      if (!ok) { stop = true; return v; }
+      tc_fence_after();
+      return fmaxf(v, __uint_as_float(tmem_ld1(col + (1 - half))));
+    };
+    // combine a per-head value with the other half's: both halves' warps reach the same
+    // TMEM lanes, so the value goes through a TMEM column (bounded 8-warp exchange)
     auto exchange = [&](float v) -> float {
-      float* slot = mx + (nsync & 1) * 256;
-      slot[half * 128 + h] = v;
+      const uint32_t col = lane_base + kXCol + 2 * (nsync & 1);
+      tmem_st1(col + half, __float_as_uint(v));
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(hsync);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(hsync, nsync & 1, abort_flag, p.status,
                                                         DSA_FLAG_TIMEOUT));
       ++nsync;
       if (!ok) { stop = true; return 0.f; }
-      return slot[(1 - half) * 128 + h];
+      tc_fence_after();
+      return __uint_as_float(tmem_ld1(col + (1 - half)));
     };
     for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
       const int t = u / p.nsplit, sp = u - t * p.nsplit;
@@ -422,79 +538,48 @@ sfa_tc_kernel(Params p) {
       unit_range(nv, sp, p.nsplit, lo, n);
       const int nch = (n + kNC - 1) / kNC;
       float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the sum
+      const int g0 = gc;
+      uint32_t cur[16], nxt[16];  // this thread's staged fp16 partials (32 columns)
+      if (nch > 0 && !stage(g0, cur)) break;
       for (int c = 0; c < nch; ++c, ++gc) {
+        // stage the next chunk first when its logits are already there, so its exchange is
+        // in flight while this one is processed; otherwise process this one first
+        bool early = false;
+        if (c + 1 < nch) {
+          early = __all_sync(0xffffffffu, mbar_test(smem_u32(s_full), (gc + 1) & 1));
+          if (early && !stage(gc + 1, nxt)) { stop = true; break; }
+        }
         const int rows_in = min(kNC, n - c * kNC);
         const int xb = gc & 1;               // exchange buffer
         const uint32_t xph = (gc >> 1) & 1;  // parity of its use count
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full, gc & 1, abort_flag, p.status,
-                                               DSA_FLAG_TIMEOUT))) { stop = true; break; }
-        tc_fence_after();
-        float s[64];
-        {
-          uint32_t r[32];
-          tmem_ld32(lane_base + kSCol, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
-          tmem_ld32(lane_base + kSCol + 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty);
-        // push our half of the partial logits, scaled to log2 units and rounded to fp16, into
-        // the peer's buffer ([8][128] x 8 halves; the bytes complete on the peer's x_full),
-        // then read the peer's 64 from ours.  The link between the two SMs moves ~12 B per
-        // clock, so the exchange is half the time it would be in fp32; fp16 keeps 2^-11
-        // relative precision, below the bf16 rounding that P gets anyway.
-        if (leader) mbar_arrive_expect_tx(&x_full[xb], kXBytes);
-        if (!__all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xph ^ 1, abort_flag, p.status,
-                                               DSA_FLAG_TIMEOUT))) {
-          stop = true; break;
-        }
-        const uint32_t xdst = xs_peer + (uint32_t)(xb * kXBytes);
-        const uint32_t xbar = x_full_peer + (uint32_t)(xb * 8);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = 8 * q + 2 * e;
-            const float a = (half ? s[32 + i0] : s[i0]) * p.scale_log2;
-            const float b = (half ? s[33 + i0] : s[i0 + 1]) * p.scale_log2;
-            const __half2 h2 = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f),
-                                                 fminf(fmaxf(b, -65504.f), 65504.f));
-            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          st_async_u4(xdst + (uint32_t)(((4 * half + q) * kH + h) * 16),
-                      make_uint4(w[0], w[1], w[2], w[3]), xbar);
-        }
-        // CTA-scope wait: the peer's st.async bytes complete on this CTA's own mbarrier (as a
-        // TMA write would), and polling with cluster-scope acquire stalls the tensor core
         if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xb], xph, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
-        const uint4* xin = xs + xb * (kXBytes / 16);
+        // logits of this thread's 32 columns = its CTA's fp16 partial + the peer's (fp16 + fp16
+        // is the same sum in both CTAs, so both take the same softmax decisions)
+        const uint4* oth = xs + xb * (kXBytes / 16);
+        float s[32];
         float m_c = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 x4 = xin[q * kH + h];
-          const uint32_t wv[4] = {x4.x, x4.y, x4.z, x4.w};
+        for (int q = 0; q < 4; ++q) {
+          const uint4 b4 = oth[(4 * half + q) * kH + h];
+          const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 o2 = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&cur[4 * q + e]));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
             const int i = 8 * q + 2 * e;
-            const float x0 = fmaf(s[i], p.scale_log2, o2.x);
-            const float x1 = fmaf(s[i + 1], p.scale_log2, o2.y);
-            s[i] = i < rows_in ? x0 : -INFINITY;
-            s[i + 1] = i + 1 < rows_in ? x1 : -INFINITY;
+            s[i] = 32 * half + i < rows_in ? fa.x + fb.x : -INFINITY;
+            s[i + 1] = 32 * half + i + 1 < rows_in ? fa.y + fb.y : -INFINITY;
             m_c = fmaxf(m_c, fmaxf(s[i], s[i + 1]));
           }
         }
         __syncwarp();
-        // the reads above fed m_c: the buffer may be refilled
+        // the reads above fed m_c: the peer may refill the buffer
         if (lane == 0) mbar_arrive_remote_relaxed(x_empty_peer + (uint32_t)(xb * 8));
+        m_c = pair_max(m_c, gc);  // the same chunk maximum in both halves
+        if (stop) break;
         // running max: move the reference only when it grows by more than 2^8
         const bool grow = m_c > m_ref + kRescaleLog2;
         const float m_new = grow ? m_c : m_ref;
@@ -518,8 +603,8 @@ sfa_tc_kernel(Params p) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float x0 = half ? s[32 + 2 * i] : s[2 * i];
-          const float x1 = half ? s[33 + 2 * i] : s[2 * i + 1];
+          const float x0 = s[2 * i];
+          const float x1 = s[2 * i + 1];
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(x0 - m_ref), ex2(x1 - m_ref));
           const float2 f2 = __bfloat1622float2(b2);
           l += f2.x + f2.y;
@@ -532,6 +617,9 @@ sfa_tc_kernel(Params p) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
+        if (c + 1 < nch && !early && !stage(gc + 1, nxt)) { stop = true; break; }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
       }
       if (stop) break;
 
@@ -704,11 +792,14 @@ bool sfa_tc_eligible(const SfaArgs& a) {
 // unit: the merge may stage the partner's partial in the idle ring and exchange buffers.
 int sfa_tc_nsplit(int total_q) { return total_q > 0 && num_sms() >= 4 * total_q ? 2 : 1; }
 
+// Per-CTA compacted key-row lists (the grid has at most num_sms CTAs), then, with a
+// split, the partial (O, m, l) slots and the per-row arrival counters.
 size_t sfa_tc_scratch_bytes(int total_q) {
+  const size_t lists = align_up((size_t)num_sms() * kMaxTopK * 4, 256);
   const int ns = sfa_tc_nsplit(total_q);
-  if (ns == 1) return 0;
+  if (ns == 1) return lists;
   const size_t slots = (size_t)total_q * ns * 2;
-  return align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256) +
+  return lists + align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256) +
          align_up((size_t)total_q * 2 * 4, 256);
 }
 
@@ -727,9 +818,11 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   p.out = a.out;
   p.lse = a.lse;
   p.status = a.status;
+  char* b = static_cast<char*>(scratch);
+  p.lists = reinterpret_cast<int32_t*>(b);
+  b += align_up((size_t)num_sms() * kMaxTopK * 4, 256);
   if (ns > 1) {
     const size_t slots = (size_t)a.seqs.total_q * ns * 2;
-    char* b = static_cast<char*>(scratch);
     p.part_o = reinterpret_cast<float4*>(b);
     b += align_up(slots * kH * 256 * 4, 256);
     p.part_ml = reinterpret_cast<float*>(b);
