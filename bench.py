@@ -262,16 +262,24 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # timed steps: no per-kernel events in the stream, so each kernel may start while the
+    # one before it finishes (programmatic dependent launch)
     with ClockSampler(local) as clk:
-        with dsa.trace(capacity=64 * args.steps) as tr:
-            for i in range(args.steps):
-                flush.zero_()
-                evs[i][0].record()
-                step()
-                evs[i][1].record()
-            torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record()
+            step()
+            evs[i][1].record()
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    # a second pass of the same steps with CUDA events around every launch (on its stream):
+    # per-kernel durations for the roofline and the launch count
+    with dsa.trace(capacity=64 * args.steps) as tr:
+        for i in range(args.steps):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = sum(step_ms)
     t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)

@@ -313,11 +313,16 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
   return run_topk(ta, s);
 }
 
+SfaArgs sfa_args(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx,
+                 void* out, float* lse, void* ws) {
+  return SfaArgs{seqs_of(p), p->h, p->d_c, p->d_rope, p->top_k, p->kv_dtype, p->out_dtype,
+                 scale_of(p), q, kv, idx, out, lse, static_cast<uint32_t*>(ws)};
+}
+
 int run_sfa(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx, void* out,
-            float* lse, void* ws, void* scratch, cudaStream_t s) {
-  SfaArgs sa{seqs_of(p), p->h, p->d_c, p->d_rope, p->top_k, p->kv_dtype, p->out_dtype,
-             scale_of(p), q, kv, idx, out, lse, static_cast<uint32_t*>(ws)};
-  if (sfa_tc_eligible(sa)) return launch_sfa_tc(sa, scratch, s);
+            float* lse, void* ws, void* scratch, cudaStream_t s, bool counters_zeroed = false) {
+  const SfaArgs sa = sfa_args(p, q, kv, idx, out, lse, ws);
+  if (sfa_tc_eligible(sa)) return launch_sfa_tc(sa, scratch, s, counters_zeroed);
   return launch_sfa_simt(sa, s);
 }
 
@@ -442,8 +447,13 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
   IndexerScratch sc;
   carve_indexer(p, ws, &sc);
   int32_t* idx = idx_out ? idx_out : sc.idx;
+  // the attention kernel's counters are cleared first, so the three kernels run back to
+  // back (each may start while the one before it finishes)
+  const SfaArgs sa = sfa_args(p, q, kv, idx, out, lse, ws);
+  const bool tc = sfa_tc_eligible(sa);
+  if (tc) DSA_TRY(sfa_tc_clear_counters(sa, sc.sfa, s));
   DSA_TRY(run_fused_indexer(p, q_idx, k_idx, w, q_scale, k_scale, idx, vals_out, ws, s));
-  return run_sfa(p, q, kv, idx, out, lse, ws, sc.sfa, s);
+  return run_sfa(p, q, kv, idx, out, lse, ws, sc.sfa, s, tc);
 }
 
 int dsa_clear_status(void* ws, void* stream) {

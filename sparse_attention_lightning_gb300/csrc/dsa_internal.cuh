@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dsa.h"
 
 namespace dsa {
@@ -100,6 +102,31 @@ int num_sms();
   } while (0)
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the
+// kernel before it in the stream is still running; it must run griddep_wait() before it
+// reads anything that kernel writes.  griddep_launch() lets the next such kernel start.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// ----------------------------------------------------------------------------
 // Kernel launchers (each defined in its own .cu).
 struct IndexerArgs {
   Seqs seqs;
@@ -165,6 +192,10 @@ int launch_sfa_simt(const SfaArgs& a, cudaStream_t stream);
 // tcgen05 SFA (H = 128, d_c = 512, d_rope = 64, bf16) on 2-CTA clusters.
 bool sfa_tc_eligible(const SfaArgs& a);
 size_t sfa_tc_scratch_bytes(int total_q);
-int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream);
+int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream,
+                  bool counters_zeroed = false);
+// Zero the split-row arrival counters of the tensor-core path ahead of time (so that no
+// memset separates the kernels of a fused call); a no-op without a split.
+int sfa_tc_clear_counters(const SfaArgs& a, void* scratch, cudaStream_t stream);
 
 }  // namespace dsa

@@ -226,6 +226,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch();  // the Top-K kernel may be scheduled (it waits)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------

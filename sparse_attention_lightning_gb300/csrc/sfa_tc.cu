@@ -225,6 +225,9 @@ sfa_tc_kernel(Params p) {
                         k1 <= p.seqs.total_k && k1 - k0 <= p.seqs.max_k_len;
         // valid entries of idx[t, :] in slot order -> list (absolute key rows).  Each lane
         // owns a contiguous run of up to 64 slots, loaded all at once (independent loads).
+        // The Top-K kernel that writes idx may still be running: wait for it here, after
+        // the work that does not depend on it.
+        griddep_wait();
         const int32_t* irow = p.idx + (int64_t)t * p.top_k;
         const int seg = (p.top_k + 31) / 32;
         const int s0 = lane * seg;
@@ -803,7 +806,18 @@ size_t sfa_tc_scratch_bytes(int total_q) {
          align_up((size_t)total_q * 2 * 4, 256);
 }
 
-int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
+int sfa_tc_clear_counters(const SfaArgs& a, void* scratch, cudaStream_t stream) {
+  const int ns = sfa_tc_nsplit(a.seqs.total_q);
+  if (ns == 1 || a.seqs.total_q == 0) return DSA_OK;
+  const size_t slots = (size_t)a.seqs.total_q * ns * 2;
+  char* b = static_cast<char*>(scratch) + align_up((size_t)num_sms() * kMaxTopK * 4, 256) +
+            align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256);
+  cudaError_t e = cudaMemsetAsync(b, 0, (size_t)a.seqs.total_q * 2 * 4, stream);
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
+  return DSA_OK;
+}
+
+int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream, bool counters_zeroed) {
   if (a.seqs.total_q == 0) return DSA_OK;
   const int ns = sfa_tc_nsplit(a.seqs.total_q);
   Params p{};
@@ -828,8 +842,10 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
     p.part_ml = reinterpret_cast<float*>(b);
     b += align_up(slots * kH * 2 * 4, 256);
     p.counters = reinterpret_cast<int*>(b);
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, (size_t)a.seqs.total_q * 2 * 4, stream);
-    if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
+    if (!counters_zeroed) {
+      const int rc = sfa_tc_clear_counters(a, scratch, stream);
+      if (rc != DSA_OK) return rc;
+    }
   }
   if (cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
@@ -837,8 +853,10 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   const int64_t units = (int64_t)a.seqs.total_q * ns;
   const int max_clusters = num_sms() / 2;
   const int clusters = (int)(units < max_clusters ? units : max_clusters);
+  cudaError_t e = cudaSuccess;
   DSA_LAUNCH("sfa_tc", stream,
-             sfa_tc_kernel<<<2 * clusters, kThreads, kSmem, stream>>>(p));
+             e = launch_pdl(sfa_tc_kernel, dim3(2 * clusters), dim3(kThreads), kSmem, stream, p));
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
   return check_launch("sfa_tc");
 }
 

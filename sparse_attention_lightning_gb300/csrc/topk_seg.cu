@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kT, 1) topk_seg_kernel(TopkArgs a, int32_t* bu
   if (s0 >= n) return;
   const int nseg = (n + kSeg - 1) / kSeg;
   const int k = min(a.top_k, n);
+  griddep_wait();                          // the scores and histograms are complete
+  if (tid == 0) griddep_launch();          // the attention kernel may be scheduled (it waits)
   const float* row = a.scores + (int64_t)t * a.ld;
   int32_t* irow = a.idx + (int64_t)t * a.top_k;
   float* vrow = a.vals ? a.vals + (int64_t)t * a.top_k : nullptr;
@@ -300,8 +302,11 @@ int launch_topk_seg(const TopkArgs& a, int32_t* buf, int64_t buf_ld, uint32_t* s
                            (int)smem) != cudaSuccess)
     return check_launch("topk_seg: smem attribute");
   dim3 grid(a.seqs.total_q, nseg);  // rows on x (up to 2^31 - 1), segments on y
+  cudaError_t e = cudaSuccess;
   DSA_LAUNCH("topk_seg", stream,
-             topk_seg_kernel<<<grid, kT, smem, stream>>>(a, buf, buf_ld, seg_counts, nseg, done));
+             e = launch_pdl(topk_seg_kernel, grid, dim3(kT), smem, stream, a, buf, buf_ld,
+                            seg_counts, nseg, done));
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "topk_seg: %s", cudaGetErrorString(e));
   return check_launch("topk_seg");
 }
 
