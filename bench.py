@@ -33,6 +33,29 @@ METRIC = "DSA tokens/sec (decode, prefill) on 1 GB300; % HBM and tensor-core roo
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from one ncu capture
+# summarised under profiles/, valid only for the kernel sources it was taken with: a change to
+# any of them (their hash differs) makes the figure unknown again.
+MEASURED_TRAFFIC = {
+    # (kernel, workload): (bytes per launch, sources, sha256 prefix of the sources)
+    ("sfa_tc", "decode"): (84_738_560, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                           "8d62f8db17fb287e"),
+}
+
+
+def measured_traffic(kernel: str, workload: str):
+    ent = MEASURED_TRAFFIC.get((kernel, workload))
+    if ent is None:
+        return None
+    nbytes, files, digest = ent
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "sparse_attention_lightning_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest().startswith(digest) else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -303,14 +326,16 @@ def main():
         alg = model[stage]["bytes"] if stage in model else cfg.total_q * cfg.top_k * 4
         achieved = alg / (dom_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": dom,
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": measured_traffic(dom, args.workload), "kernel": dom,
                 "algorithmic_bytes_per_launch": alg, "peak_source": f"{peak_src} hbm_gbs"}
     else:
         alg = model[stage]["flops"]
         achieved = alg / (dom_ms / 1e3) / 1e12
         pk = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": None, "kernel": dom,
+                "frac": achieved / pk, "traffic": measured_traffic(dom, args.workload),
+                "kernel": dom,
                 "algorithmic_flops_per_launch": alg, "peak_source": f"{peak_src} bf16_tflops"}
     roof["kernel_ms_mean"] = dom_ms
     kernels = {k: {"launches": len(v), "ms_mean": statistics.mean(v),
