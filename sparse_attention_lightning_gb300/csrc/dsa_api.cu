@@ -307,6 +307,7 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
     DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, ld, s));
   }
   TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws), hist};
+  if (hist && topk_cluster_eligible(ta)) return launch_topk_cluster(ta, s);
   if (hist)
     return launch_topk_seg(ta, sc.segbuf, segbuf_ld(p), sc.segcnt,
                            hist + (size_t)p->total_q * kHistBins, s);

@@ -173,6 +173,9 @@ int launch_topk_smem(const TopkArgs& a, cudaStream_t stream);
 // done [total_q] zero on entry (left zero).
 int topk_seg_segments(int max_k_len);
 int topk_seg_max_keys();
+// One thread-block cluster (up to 8 CTAs) per row, histogram-seeded (a.hist set).
+bool topk_cluster_eligible(const TopkArgs& a);
+int launch_topk_cluster(const TopkArgs& a, cudaStream_t stream);
 int launch_topk_seg(const TopkArgs& a, int32_t* buf, int64_t buf_ld, uint32_t* seg_counts,
                     uint32_t* done, cudaStream_t stream);
 
