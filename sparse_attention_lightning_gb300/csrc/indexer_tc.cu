@@ -7,23 +7,30 @@
 // LLMs", §4.1: batched dot product of the indexer query with the K cache, then
 // the weighted sum over heads, read straight from the K cache.)
 //
-// Work unit: one query row t × one tile of 128 keys.  The tile is the MMA's
-// M = 128 (one key per TMEM lane), the row's 64 heads are N = 64, K = d_I.
+// Work unit: a block of QB consecutive query rows of one sequence × one tile of 128
+// keys.  The tile is the MMA's M = 128 (one key per TMEM lane), the block's QB × 64
+// heads are N, K = d_I.  Decode uses QB = 1 (N = 64); prefill uses QB = 4: N = 256
+// runs the tensor core at its full rate (an N = 64 MMA takes 46 clocks for a quarter of
+// the work an N = 256 one does in 128) and each key tile read from L2 serves four
+// query rows instead of one.
 // The per-head logits z[t, j, s] exist only in tensor memory: the epilogue
 // reads its key's 64 columns and reduces them to one score (ReLU, · w, Σ_j)
 // without any cross-thread reduction.  For FP8 the scales fold in as
 // I = k_scale[s] · Σ_j (w·q_scale)[t,j] · ReLU(z8) (all scales are positive).
 //
-// Schedule: the tiles of all rows are laid end to end (a causal row at
-// position p has floor(p/128) + 1 of them) and each persistent CTA takes one
-// contiguous, equal share, so a long-history row is simply spread over more
-// CTAs than a short one.  Each CTA derives the tile layout itself from cu_q /
-// cu_k: per sequence the tile count is F(L) - F(L - T) with
+// Schedule: the tiles of all blocks are laid end to end (a block whose last row
+// sits at position p has floor(p/128) + 1 of them) and each persistent CTA takes
+// one contiguous, equal share, so a long-history block is simply spread over more
+// CTAs than a short one.  Each CTA derives the tile layout itself from cu_q / cu_k
+// in closed form.  QB = 1: per sequence F(L) - F(L - T) with
 // F(n) = Σ_{p<n} (floor(p/128) + 1) = n + 64 q (q - 1) + r q  (q = n / 128, r = n % 128).
-// Warp roles: warp 0 issues TMA loads (a 4-8 stage ring of key tiles, a 2-slot
-// ring of query blocks), warp 1 owns TMEM and issues the MMAs, warps 2..5 run
-// the epilogue on a double-buffered TMEM accumulator.  Every wait is bounded
-// (DSA_FLAG_TIMEOUT).
+// QB = 4: the first nb full blocks of a sequence hold nb + G(a + nb) - G(a) tiles,
+// a = (L - T + 3) / 4, G(n) = Σ_{x<n} floor(x/32); a partial last block holds
+// floor((L-1)/128) + 1.
+// Warp roles: warp 0 issues TMA loads (a ring of key tiles, query blocks), warp 1
+// owns TMEM and issues the MMAs, the other warps run the epilogue on a
+// double-buffered TMEM accumulator (QB = 4: two warps per TMEM lane quarter, each
+// taking two of the block's rows).  Every wait is bounded (DSA_FLAG_TIMEOUT).
 #include "dsa_internal.cuh"
 #include "tc_sm100.cuh"
 
@@ -34,23 +41,35 @@ using namespace tc;
 
 constexpr int kMaxSeqs = 4096;  // sequences per launch on this path (tile table in smem)
 
-template <bool FP8>
+template <bool FP8, int QB>
 struct Cfg {
   static constexpr int BM = 128;   // keys per tile (MMA M)
-  static constexpr int HI = 64;    // heads (MMA N)
+  static constexpr int HI = 64;    // heads per query row
+  static constexpr int N = HI * QB;  // MMA N: the block's heads
   static constexpr int DI = 128;   // head width (MMA K total)
   static constexpr int ES = FP8 ? 1 : 2;
   static constexpr int ROWB = DI * ES;             // bytes per key row (128 or 256)
   static constexpr int ATOMS = ROWB / 128;         // 128-byte swizzle atoms per row
   static constexpr int KTILE = BM * ROWB;          // 32 KB bf16, 16 KB fp8
-  static constexpr int QTILE = HI * ROWB;          // 16 KB bf16, 8 KB fp8
-  static constexpr int NS = FP8 ? 8 : 4;           // key-tile stages
+  static constexpr int QTILE = N * ROWB;           // one query block
+  static constexpr int NQ = QB == 1 ? 2 : 1;       // query-block buffers
+  static constexpr int NS = QB == 1 ? (FP8 ? 8 : 4) : (FP8 ? 6 : 3);  // key-tile stages
   static constexpr int KSTEPS = FP8 ? 4 : 8;       // MMAs per tile (32 B of K each)
-  static constexpr int ACC_COLS = HI;              // fp32 accumulator columns
+  static constexpr int ACC_COLS = N;               // fp32 accumulator columns
   static constexpr int TMEM_COLS = 2 * ACC_COLS;   // double buffered
-  static constexpr int SMEM_FIXED = NS * KTILE + 2 * QTILE + kHistBins * 4 + 2048 /*bars etc*/ +
-                                    1024 /*align*/;
+  static constexpr int EPI_WARPS = QB == 1 ? 4 : 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int RPW = QB * 4 / EPI_WARPS;   // query rows per epilogue warp
+  // per-row histograms: 32-bit counters for one row, 16-bit ones (flushed before they
+  // can overflow) for a block of four
+  static constexpr int HIST_BYTES = QB == 1 ? kHistBins * 4 : QB * kHistBins * 2;
+  static constexpr int MISC = 256 /*barriers*/ + EPI_WARPS * RPW * HI * 4 /*weights*/ + 64;
+  static constexpr int SMEM_FIXED = NS * KTILE + NQ * QTILE + HIST_BYTES + MISC + 1024 /*align*/;
+  static_assert(TMEM_COLS <= 512, "TMEM");
 };
+
+constexpr int kQBMaxSeqs = 64;   // sequences per launch of the QB = 4 kernel (table in smem)
+constexpr int kFlushItems = 256; // QB = 4: tiles between flushes (a 16-bit bin grows <= 128 a tile)
 
 struct Params {
   Seqs seqs;
@@ -68,6 +87,28 @@ __device__ __forceinline__ int64_t ftiles(int64_t n) {  // Σ_{p<n} (floor(p/128
   return n + 64 * q * (q - 1) + r * q;
 }
 
+// Σ_{x<n} floor(x / D)
+__device__ __forceinline__ int64_t gsum(int64_t n, int64_t D) {
+  const int64_t q = n / D, r = n % D;
+  return D * q * (q - 1) / 2 + r * q;
+}
+
+// Tiles of the first nb blocks of a sequence with T queries over L keys (nb <= full blocks).
+template <int QB>
+__device__ __forceinline__ int64_t block_tiles(int T, int L, int nb) {
+  if (QB == 1) return ftiles(L - T + nb) - ftiles(L - T);
+  const int64_t a = (L - T + QB - 1) / QB;
+  return nb + gsum(a + nb, 128 / QB) - gsum(a, 128 / QB);
+}
+
+// All tiles of a sequence.
+template <int QB>
+__device__ __forceinline__ int64_t seq_tiles(int T, int L) {
+  if (QB == 1) return ftiles(L) - ftiles(L - T);
+  const int nfull = T / QB;
+  return block_tiles<QB>(T, L, nfull) + (T % QB ? (L - 1) / 128 + 1 : 0);
+}
+
 // Per-sequence tile table built in shared memory by every CTA.
 struct SeqTab {
   const int32_t* st;  // [B+1] first tile of each sequence, then the total
@@ -76,19 +117,22 @@ struct SeqTab {
   int B;
 };
 
-// Walks the CTA's items (row tile by row tile) in order; all roles run one.
+// Walks the CTA's items (block tile by block tile) in order; all roles run one.
+template <int QB>
 struct Cursor {
-  int b, i, T, L, q0, k0;  // sequence, query index in it, its sizes and offsets
-  int t, pos, j, ntiles;   // packed row, its position, current tile, tiles of the row
+  int b, ib, T, L, q0, k0;   // sequence, block index in it, its sizes and offsets
+  int t, pos, nrow, j, ntiles;  // first packed row of the block, its position, rows, tile
 
   __device__ __forceinline__ void load_seq(const SeqTab& s) {
     q0 = s.cq[b]; T = s.cq[b + 1] - q0;
     k0 = s.ck[b]; L = s.ck[b + 1] - k0;
   }
-  __device__ __forceinline__ void set_row() {
-    t = q0 + i;
-    pos = L - T + i;
-    ntiles = pos / 128 + 1;
+  __device__ __forceinline__ void set_block() {
+    const int i0 = QB * ib;
+    t = q0 + i0;
+    pos = L - T + i0;
+    nrow = min(QB, T - i0);
+    ntiles = (pos + nrow - 1) / 128 + 1;
   }
   __device__ __forceinline__ void locate(const SeqTab& s, int g) {
     int lo = 0, hi = s.B - 1;  // last b with st[b] <= g
@@ -98,29 +142,33 @@ struct Cursor {
     }
     b = lo;
     load_seq(s);
-    const int64_t gl = g - s.st[b], base = ftiles(L - T);
-    int ilo = 0, ihi = T - 1;  // last i with F(L - T + i) - base <= gl
+    const int64_t gl = g - s.st[b];
+    const int nfull = T / QB, nblk = (T + QB - 1) / QB;
+    int ilo = 0, ihi = nblk - 1;  // last block whose first tile is <= gl
     while (ilo < ihi) {
       const int mid = (ilo + ihi + 1) >> 1;
-      if (ftiles(L - T + mid) - base <= gl) ilo = mid; else ihi = mid - 1;
+      const int64_t before = mid <= nfull ? block_tiles<QB>(T, L, mid) : INT64_MAX;
+      if (before <= gl) ilo = mid; else ihi = mid - 1;
     }
-    i = ilo;
-    set_row();
-    j = (int)(gl - (ftiles(L - T + i) - base));
+    ib = ilo;
+    set_block();
+    j = (int)(gl - block_tiles<QB>(T, L, min(ib, nfull)));
   }
   __device__ __forceinline__ void advance(const SeqTab& s) {
     if (++j < ntiles) return;
     j = 0;
-    if (++i == T) {
-      i = 0;
+    if (++ib * QB >= T) {
+      ib = 0;
       do { ++b; } while (b < s.B - 1 && s.st[b + 1] == s.st[b]);  // skip tile-less sequences
       load_seq(s);
     }
-    set_row();
+    set_block();
   }
 };
 
-__device__ __forceinline__ uint32_t scan192(uint32_t v, uint32_t* ws, uint32_t* total) {
+// Block-wide exclusive prefix sum over NW warps (two barriers).
+template <int NW>
+__device__ __forceinline__ uint32_t scan_block(uint32_t v, uint32_t* ws, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -131,7 +179,7 @@ __device__ __forceinline__ uint32_t scan192(uint32_t v, uint32_t* ws, uint32_t* 
   if (lane == 31) ws[warp] = x;
   __syncthreads();
   uint32_t before = 0, tot = 0;
-  for (int w = 0; w < 6; ++w) {
+  for (int w = 0; w < NW; ++w) {
     if (w < warp) before += ws[w];
     tot += ws[w];
   }
@@ -140,17 +188,18 @@ __device__ __forceinline__ uint32_t scan192(uint32_t v, uint32_t* ws, uint32_t* 
   return before + x - v;
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(192, 1)
+template <bool FP8, int QB>
+__global__ void __launch_bounds__(Cfg<FP8, QB>::THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   Params p) {
-  using C = Cfg<FP8>;
+  using C = Cfg<FP8, QB>;
+  constexpr int EPI_THREADS = 32 * C::EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* ks = smem;                                  // NS key tiles
-  uint8_t* qs = ks + C::NS * C::KTILE;                 // 2 query blocks
-  uint32_t* hs = reinterpret_cast<uint32_t*>(qs + 2 * C::QTILE);  // row-segment histogram
-  uint64_t* bars = reinterpret_cast<uint64_t*>(hs + kHistBins);
+  uint8_t* qs = ks + C::NS * C::KTILE;                 // NQ query blocks
+  uint32_t* hs = reinterpret_cast<uint32_t*>(qs + C::NQ * C::QTILE);  // row-segment histograms
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(hs) + C::HIST_BYTES);
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* q_full = k_empty + C::NS;
@@ -158,12 +207,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   uint64_t* acc_full = q_empty + 2;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint64_t* epi_a = drain + 1;     // 128 epilogue threads: row segment scored
-  uint64_t* epi_b = drain + 2;     // 128 epilogue threads: histogram flushed
-  float* wsm = reinterpret_cast<float*>(drain + 4);  // [4 epilogue warps][64]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsm + 4 * 64);
+  uint64_t* epi_a = drain + 1;     // the epilogue threads: row segment scored
+  uint64_t* epi_b = drain + 2;     // the epilogue threads: histograms flushed
+  float* wsm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [warps][RPW][64]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsm + C::EPI_WARPS * C::RPW * C::HI);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint32_t* scan_ws = tmem_slot + 2;                   // [6]
+  uint32_t* scan_ws = tmem_slot + 2;                   // [THREADS / 32]
   int32_t* tab = reinterpret_cast<int32_t*>(smem + C::SMEM_FIXED - 1024);
   const int B = p.seqs.B;
   int32_t* st = tab;
@@ -174,7 +223,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
   // ---- tile table of the sequences (every CTA builds its own copy) ----
   uint32_t carry = 0;
-  for (int base = 0; base < B; base += 192) {
+  for (int base = 0; base < B; base += C::THREADS) {
     const int b = base + threadIdx.x;
     uint32_t n = 0;
     if (b < B) {
@@ -183,18 +232,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       const int T = q1 - q0, L = k1 - k0;
       const bool ok = q0 >= 0 && T >= 0 && T <= L && k0 >= 0 && k1 <= p.seqs.total_k &&
                       L <= p.seqs.max_k_len && q1 <= p.seqs.total_q;
-      if (ok) n = (uint32_t)(ftiles(L) - ftiles(L - T));
+      if (ok) n = (uint32_t)seq_tiles<QB>(T, L);
       else if (blockIdx.x == 0) atomicOr(p.status, DSA_FLAG_BAD_SEQS);
       cq[b] = q0;
       ck[b] = k0;
     }
     uint32_t tot;
-    const uint32_t excl = scan192(n, scan_ws, &tot);
+    const uint32_t excl = scan_block<C::THREADS / 32>(n, scan_ws, &tot);
     if (b < B) st[b] = (int32_t)(carry + excl);
     carry += tot;
   }
   if (p.hist)
-    for (int i = threadIdx.x; i < kHistBins; i += 192) hs[i] = 0u;
+    for (int i = threadIdx.x; i < C::HIST_BYTES / 4; i += C::THREADS) hs[i] = 0u;
   if (threadIdx.x == 0) {
     st[B] = (int32_t)carry;
     cq[B] = __ldg(p.seqs.cu_q + B);
@@ -211,11 +260,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     for (int i = 0; i < C::NS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
-      mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], C::EPI_WARPS);
     }
     mbar_init(drain, 1);
-    mbar_init(epi_a, 128);
-    mbar_init(epi_b, 128);
+    mbar_init(epi_a, EPI_THREADS);
+    mbar_init(epi_b, EPI_THREADS);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&kmap);
@@ -232,20 +281,20 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      Cursor cur;
+      Cursor<QB> cur;
       cur.locate(tabs, g0);
-      int rows_seen = 0, issued = 0;
+      int blocks_seen = 0, issued = 0;
       for (int g = g0, it = 0; g < g1; ++g, ++it) {
         if (g > g0) cur.advance(tabs);
         if (g == g0 || cur.j == 0) {
-          const int slot = rows_seen & 1;
-          if (!mbar_wait(&q_empty[slot], ((rows_seen >> 1) & 1) ^ 1, abort_flag, p.status,
+          const int slot = blocks_seen % C::NQ;
+          if (!mbar_wait(&q_empty[slot], ((blocks_seen / C::NQ) & 1) ^ 1, abort_flag, p.status,
                          DSA_FLAG_TIMEOUT)) break;
           mbar_arrive_expect_tx(&q_full[slot], C::QTILE);
           for (int a = 0; a < C::ATOMS; ++a)
-            tma_load_2d(qs + slot * C::QTILE + a * (C::HI * 128), &qmap, &q_full[slot],
+            tma_load_2d(qs + slot * C::QTILE + a * (C::N * 128), &qmap, &q_full[slot],
                         a * (128 / C::ES), cur.t * C::HI);
-          ++rows_seen;
+          ++blocks_seen;
         }
         const int s = it % C::NS;
         if (!mbar_wait(&k_empty[s], ((it / C::NS) & 1) ^ 1, abort_flag, p.status,
@@ -256,28 +305,28 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                            a * (128 / C::ES), cur.k0 + cur.j * C::BM, pol);
         issued = it + 1;
       }
-      // every key-tile copy issued has landed before the CTA may exit
+      // every copy issued has landed before the CTA may exit
       for (int i = (issued > C::NS ? issued - C::NS : 0); i < issued; ++i)
         mbar_wait_drain(&k_full[i % C::NS], (i / C::NS) & 1);
-      if (rows_seen > 0) mbar_wait_drain(&q_full[(rows_seen - 1) & 1], ((rows_seen - 1) >> 1) & 1);
-      if (rows_seen > 1) mbar_wait_drain(&q_full[(rows_seen - 2) & 1], ((rows_seen - 2) >> 1) & 1);
+      for (int i = (blocks_seen > C::NQ ? blocks_seen - C::NQ : 0); i < blocks_seen; ++i)
+        mbar_wait_drain(&q_full[i % C::NQ], (i / C::NQ) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = FP8 ? idesc_e4m3(128, C::HI) : idesc_bf16(128, C::HI);
-      Cursor cur;
+      const uint32_t idesc = FP8 ? idesc_e4m3(128, C::N) : idesc_bf16(128, C::N);
+      Cursor<QB> cur;
       cur.locate(tabs, g0);
-      int rows_seen = 0;
+      int blocks_seen = 0;
       for (int g = g0, it = 0; g < g1; ++g, ++it) {
         if (g > g0) cur.advance(tabs);
         if (g == g0 || cur.j == 0) {
-          if (!mbar_wait(&q_full[rows_seen & 1], (rows_seen >> 1) & 1, abort_flag, p.status,
-                         DSA_FLAG_TIMEOUT)) break;
+          if (!mbar_wait(&q_full[blocks_seen % C::NQ], (blocks_seen / C::NQ) & 1, abort_flag,
+                         p.status, DSA_FLAG_TIMEOUT)) break;
           tc_fence_after();
-          ++rows_seen;
+          ++blocks_seen;
         }
-        const int slot = (rows_seen - 1) & 1;
+        const int slot = (blocks_seen - 1) % C::NQ;
         const int s = it % C::NS, acc = it & 1;
         if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort_flag, p.status,
                        DSA_FLAG_TIMEOUT)) break;
@@ -289,7 +338,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
           const int atom = (kk * 32) / 128, off = (kk * 32) % 128;
           const uint64_t ad = sdesc_sw128(a0 + atom * (C::BM * 128) + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b0 + atom * (C::HI * 128) + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(b0 + atom * (C::N * 128) + off, 16, 1024);
           if (FP8) mma_e4m3(tmem + acc * C::ACC_COLS, ad, bd, idesc, kk > 0);
           else mma_bf16(tmem + acc * C::ACC_COLS, ad, bd, idesc, kk > 0);
         }
@@ -302,25 +351,32 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       mbar_wait_drain(drain, 0);
     }
   } else {
-    // ---------------- epilogue: warps 2..5, TMEM lane quarter warp % 4 ----------------
+    // ---------------- epilogue: TMEM lane quarter warp % 4, rows rgrp * RPW .. ----------------
+    const int ew = warp - 2;
     const int quarter = warp & 3;
-    const int e = threadIdx.x - 64;  // 0..127
-    float* wq = wsm + (warp - 2) * 64;
-    int nseg = 0;
-    Cursor cur;
+    const int rgrp = ew >> 2;        // QB = 4: rows {2 rgrp, 2 rgrp + 1}; QB = 1: row 0
+    const int e = threadIdx.x - 64;  // 0 .. EPI_THREADS - 1
+    float* wq = wsm + ew * C::RPW * C::HI;
+    int nseg = 0, since = 0;
+    Cursor<QB> cur;
     cur.locate(tabs, g0);
     for (int g = g0, it = 0; g < g1; ++g, ++it) {
       if (g > g0) cur.advance(tabs);
       if (g == g0 || cur.j == 0) {
         __syncwarp();
-        float w0 = __ldg(p.w + (int64_t)cur.t * C::HI + lane);
-        float w1 = __ldg(p.w + (int64_t)cur.t * C::HI + lane + 32);
-        if (FP8) {
-          w0 *= __ldg(p.q_scale + (int64_t)cur.t * C::HI + lane);
-          w1 *= __ldg(p.q_scale + (int64_t)cur.t * C::HI + lane + 32);
+#pragma unroll
+        for (int rr = 0; rr < C::RPW; ++rr) {
+          const int r = rgrp * C::RPW + rr;
+          const int64_t t = cur.t + (r < cur.nrow ? r : 0);
+          float w0 = __ldg(p.w + t * C::HI + lane);
+          float w1 = __ldg(p.w + t * C::HI + lane + 32);
+          if (FP8) {
+            w0 *= __ldg(p.q_scale + t * C::HI + lane);
+            w1 *= __ldg(p.q_scale + t * C::HI + lane + 32);
+          }
+          wq[rr * C::HI + lane] = w0;
+          wq[rr * C::HI + lane + 32] = w1;
         }
-        wq[lane] = w0;
-        wq[lane + 32] = w1;
         __syncwarp();
       }
       const int acc = it & 1;
@@ -328,34 +384,64 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                                              DSA_FLAG_TIMEOUT)))
         break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS;
-      uint32_t r[32];
-      float sum = 0.f;
-      tmem_ld32(taddr, r);
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS +
+                             rgrp * C::RPW * C::HI;
+      float sum[C::RPW];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) sum = fmaf(wq[jj], fmaxf(__uint_as_float(r[jj]), 0.f), sum);
-      tmem_ld32(taddr + 32, r);
+      for (int rr = 0; rr < C::RPW; ++rr) {
+        uint32_t r[32];
+        sum[rr] = 0.f;
+        tmem_ld32(taddr + rr * C::HI, r);
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj)
-        sum = fmaf(wq[32 + jj], fmaxf(__uint_as_float(r[jj]), 0.f), sum);
+        for (int jj = 0; jj < 32; ++jj)
+          sum[rr] = fmaf(wq[rr * C::HI + jj], fmaxf(__uint_as_float(r[jj]), 0.f), sum[rr]);
+        tmem_ld32(taddr + rr * C::HI + 32, r);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          sum[rr] = fmaf(wq[rr * C::HI + 32 + jj], fmaxf(__uint_as_float(r[jj]), 0.f), sum[rr]);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       const int s = cur.j * C::BM + quarter * 32 + lane;
-      if (s <= cur.pos) {
-        if (FP8) sum *= __ldg(p.k_scale + cur.k0 + s);
-        p.scores[(int64_t)cur.t * p.ld + s] = sum;
-        if (p.hist) atomicAdd(&hs[order_key(sum) >> 20], 1u);
+#pragma unroll
+      for (int rr = 0; rr < C::RPW; ++rr) {
+        const int r = rgrp * C::RPW + rr;
+        if (r < cur.nrow && s <= cur.pos + r) {
+          float v = sum[rr];
+          if (FP8) v *= __ldg(p.k_scale + cur.k0 + s);
+          p.scores[(int64_t)(cur.t + r) * p.ld + s] = v;
+          if (p.hist) {
+            const uint32_t bin = order_key(v) >> 20;
+            if (QB == 1) atomicAdd(&hs[bin], 1u);
+            else atomicAdd(&hs[(r * kHistBins + bin) >> 1], 1u << (16 * (bin & 1)));
+          }
+        }
       }
-      if (p.hist && (g + 1 == g1 || cur.j + 1 == cur.ntiles)) {
-        // end of this CTA's part of the row: add the segment histogram to the row's
+      const bool seg_end = g + 1 == g1 || cur.j + 1 == cur.ntiles;
+      if (p.hist && (seg_end || (QB > 1 && ++since == kFlushItems))) {
+        // add this CTA's counts to the rows' histograms, then start again from zero
+        since = 0;
         mbar_arrive(epi_a);
         if (!__all_sync(0xffffffffu, mbar_wait(epi_a, nseg & 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) break;
-        uint32_t* grow = p.hist + (int64_t)cur.t * kHistBins;
-        for (int bin = e; bin < kHistBins; bin += 128) {
-          const uint32_t v = hs[bin];
-          if (v) { atomicAdd(grow + bin, v); hs[bin] = 0u; }
+        if (QB == 1) {
+          uint32_t* grow = p.hist + (int64_t)cur.t * kHistBins;
+          for (int bin = e; bin < kHistBins; bin += EPI_THREADS) {
+            const uint32_t v = hs[bin];
+            if (v) { atomicAdd(grow + bin, v); hs[bin] = 0u; }
+          }
+        } else {
+          for (int wi = e; wi < cur.nrow * (kHistBins / 2); wi += EPI_THREADS) {
+            const uint32_t v = hs[wi];
+            if (v) {
+              const int r = wi / (kHistBins / 2), b0 = 2 * (wi % (kHistBins / 2));
+              uint32_t* grow = p.hist + (int64_t)(cur.t + r) * kHistBins;
+              if (v & 0xffffu) atomicAdd(grow + b0, v & 0xffffu);
+              if (v >> 16) atomicAdd(grow + b0 + 1, v >> 16);
+              hs[wi] = 0u;
+            }
+          }
         }
         mbar_arrive(epi_b);
         if (!__all_sync(0xffffffffu, mbar_wait(epi_b, nseg & 1, abort_flag, p.status,
@@ -373,26 +459,27 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
 }
 
-template <bool FP8>
+template <bool FP8, int QB>
 int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
-  using C = Cfg<FP8>;
+  using C = Cfg<FP8, QB>;
   CUtensorMap kmap, qmap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   int rc = make_tmap_2d(&kmap, dt, a.k_idx, C::DI, (uint64_t)a.seqs.total_k, C::ROWB,
                         128 / C::ES, C::BM);
   if (rc != DSA_OK) return rc;
   rc = make_tmap_2d(&qmap, dt, a.q_idx, C::DI, (uint64_t)a.seqs.total_q * C::HI, C::ROWB,
-                    128 / C::ES, C::HI);
+                    128 / C::ES, C::N);
   if (rc != DSA_OK) return rc;
   const int smem = C::SMEM_FIXED + (int)align_up(3 * sizeof(int32_t) * (a.seqs.B + 1), 16);
-  auto kern = indexer_tc_kernel<FP8>;
+  auto kern = indexer_tc_kernel<FP8, QB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("indexer_tc: smem attribute");
   const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + C::BM - 1) / C::BM);
   const int grid = (int)(bound < num_sms() ? bound : num_sms());
   Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status, a.hist};
-  DSA_LAUNCH(FP8 ? "indexer_tc_fp8" : "indexer_tc_bf16", stream,
-             kern<<<grid, 192, smem, stream>>>(kmap, qmap, p));
+  DSA_LAUNCH(FP8 ? (QB == 1 ? "indexer_tc_fp8" : "indexer_tc_fp8_qb4")
+                 : (QB == 1 ? "indexer_tc_bf16" : "indexer_tc_bf16_qb4"),
+             stream, kern<<<grid, C::THREADS, smem, stream>>>(kmap, qmap, p));
   return check_launch("indexer_tc");
 }
 
@@ -407,8 +494,13 @@ bool indexer_tc_eligible(const IndexerArgs& a) {
 
 int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
-  if (a.idx_dtype == DSA_FP8_E4M3) return launch_typed<true>(a, scores, ld, stream);
-  return launch_typed<false>(a, scores, ld, stream);
+  // blocks of four query rows when sequences hold several queries each (prefill)
+  const bool qb4 = a.seqs.B <= kQBMaxSeqs && a.seqs.total_q >= 4 * a.seqs.B;
+  if (a.idx_dtype == DSA_FP8_E4M3)
+    return qb4 ? launch_typed<true, 4>(a, scores, ld, stream)
+               : launch_typed<true, 1>(a, scores, ld, stream);
+  return qb4 ? launch_typed<false, 4>(a, scores, ld, stream)
+             : launch_typed<false, 1>(a, scores, ld, stream);
 }
 
 }  // namespace dsa

@@ -71,6 +71,12 @@ SMALL = [
     ([1, 1, 4], [4100, 3000, 300], dict(h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64,
                                         top_k=2048), ("e4m3", "bf16")),
     ([2, 1], [9, 65], dict(h_idx=3, d_idx=48, h=5, d_c=32, d_rope=16, top_k=5), ("e4m3", "f32")),
+    # several query rows per sequence: the indexer scores blocks of four rows at once
+    # (partial last blocks, chunked prefill T < L, a block straddling a 128-key tile edge)
+    ([37, 1, 130, 6], [300, 2500, 1300, 6], dict(h_idx=64, d_idx=128, h=128, d_c=512,
+                                                 d_rope=64, top_k=256), ("bf16", "bf16")),
+    ([37, 1, 130, 6], [300, 2500, 1300, 6], dict(h_idx=64, d_idx=128, h=128, d_c=512,
+                                                 d_rope=64, top_k=256), ("e4m3", "bf16")),
 ]
 
 
