@@ -190,27 +190,23 @@ size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 
 // starts of the tensor-core schedule.  The fused forward adds the indices.
 struct IndexerScratch {
   float* scores;
-  uint32_t* hist;       // [total_q][kHistBins] then done[total_q]: cleared per call
-  int32_t* segbuf;      // [total_q][segbuf_ld]
-  uint32_t* segcnt;     // [total_q][segments][2]
+  uint32_t* hist;       // [total_q][kHistBins]: cleared per call
+  int32_t* spill;       // [total_q][spill_ld]: a row's Top-K candidates beyond shared memory
   int32_t* idx;
   void* sfa;
 };
 
-// The tensor-core indexer also histograms each row for the segmented Top-K.
+// The tensor-core indexer also histograms each row, which seeds the Top-K kernels.
 bool use_topk_hist(const dsa_problem* p) {
   return (p->idx_dtype == DSA_BF16 || p->idx_dtype == DSA_FP8_E4M3) && p->h_idx == 64 &&
-         p->d_idx == 128 && p->max_k_len <= topk_seg_max_keys() && p->num_seqs <= 4096;
+         p->d_idx == 128 && p->num_seqs <= 4096;
 }
 size_t hist_bytes(const dsa_problem* p) {
-  return use_topk_hist(p) ? (size_t)p->total_q * (kHistBins + 1) * 4 : 0;
+  return use_topk_hist(p) ? (size_t)p->total_q * kHistBins * 4 : 0;
 }
-int64_t segbuf_ld(const dsa_problem* p) { return (int64_t)topk_seg_segments(p->max_k_len) * 8192; }
-size_t segbuf_bytes(const dsa_problem* p) {
-  return use_topk_hist(p) ? (size_t)p->total_q * segbuf_ld(p) * 4 : 0;
-}
-size_t segcnt_bytes(const dsa_problem* p) {
-  return use_topk_hist(p) ? (size_t)p->total_q * topk_seg_segments(p->max_k_len) * 8 : 0;
+int64_t spill_ld(const dsa_problem* p) { return ((int64_t)p->max_k_len + 3) / 4 * 4; }
+size_t spill_bytes(const dsa_problem* p) {
+  return use_topk_hist(p) ? (size_t)p->total_q * spill_ld(p) * 4 : 0;
 }
 
 // SFA scratch of the tensor-core path (per-CTA key-row lists, split-row partials).
@@ -223,16 +219,14 @@ size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
   const size_t o_scores = c.take(scores_bytes(p));
   const size_t o_hist = c.take(hist_bytes(p));
-  const size_t o_segbuf = c.take(segbuf_bytes(p));
-  const size_t o_segcnt = c.take(segcnt_bytes(p));
+  const size_t o_spill = c.take(spill_bytes(p));
   const size_t o_idx = c.take(idx_bytes(p));
   const size_t o_sfa = c.take(sfa_scratch_bytes(p));
   if (out) {
     char* b = static_cast<char*>(ws);
     out->scores = reinterpret_cast<float*>(b + o_scores);
     out->hist = hist_bytes(p) ? reinterpret_cast<uint32_t*>(b + o_hist) : nullptr;
-    out->segbuf = reinterpret_cast<int32_t*>(b + o_segbuf);
-    out->segcnt = reinterpret_cast<uint32_t*>(b + o_segcnt);
+    out->spill = reinterpret_cast<int32_t*>(b + o_spill);
     out->idx = reinterpret_cast<int32_t*>(b + o_idx);
     out->sfa = b + o_sfa;
   }
@@ -308,9 +302,7 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
   }
   TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws), hist};
   if (hist && topk_cluster_eligible(ta)) return launch_topk_cluster(ta, s);
-  if (hist)
-    return launch_topk_seg(ta, sc.segbuf, segbuf_ld(p), sc.segcnt,
-                           hist + (size_t)p->total_q * kHistBins, s);
+  if (hist) return launch_topk_stream(ta, sc.spill, spill_ld(p), s);
   return run_topk(ta, s);
 }
 

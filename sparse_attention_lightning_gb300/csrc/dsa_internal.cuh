@@ -168,16 +168,13 @@ int launch_topk_rows(const TopkArgs& a, cudaStream_t stream);
 // Shared-memory-resident variant for rows of at most topk_smem_max_keys() keys.
 int topk_smem_max_keys();
 int launch_topk_smem(const TopkArgs& a, cudaStream_t stream);
-// Segmented multi-CTA variant (needs a.hist): buf [total_q][buf_ld] int32 with
-// buf_ld = 8192 * topk_seg_segments(max_k_len), seg_counts [total_q][segments][2],
-// done [total_q] zero on entry (left zero).
-int topk_seg_segments(int max_k_len);
-int topk_seg_max_keys();
+// One 256-thread CTA streaming each row, histogram-seeded (a.hist set): for many rows.
+// buf [total_q][buf_ld] int32, buf_ld >= max_k_len: candidates of rows that do not fit
+// in shared memory.
+int launch_topk_stream(const TopkArgs& a, int32_t* buf, int64_t buf_ld, cudaStream_t stream);
 // One thread-block cluster (up to 8 CTAs) per row, histogram-seeded (a.hist set).
 bool topk_cluster_eligible(const TopkArgs& a);
 int launch_topk_cluster(const TopkArgs& a, cudaStream_t stream);
-int launch_topk_seg(const TopkArgs& a, int32_t* buf, int64_t buf_ld, uint32_t* seg_counts,
-                    uint32_t* done, cudaStream_t stream);
 
 struct SfaArgs {
   Seqs seqs;

@@ -127,6 +127,27 @@ def test_tensor_core_indexer_scores(idx_dtype):
     assert worst < 1e-4, worst  # fp32 accumulation of exact products: far inside 1e-2
 
 
+@pytest.mark.parametrize("all_equal", [False, True], ids=["random", "all_scores_equal"])
+def test_many_row_topk(all_equal):
+    # more than 4096 query rows: the Top-K streams each row in its own CTA.  With q_I = 0
+    # every score is 0, every key is a candidate (more than the kernel keeps in shared
+    # memory) and the tie rule alone decides: positions 0 .. k-1.
+    cfg = W.custom([4200], [4200], h_idx=64, d_idx=128, h=8, d_c=64, d_rope=16, top_k=256,
+                   idx_dtype="bf16", kv_dtype="bf16")
+    case = W.make_case(cfg, seed=41)
+    if all_equal:
+        case.q_idx.zero_()
+    P, out, lse, idx, vals = run_fused(case)
+    rng = np.random.default_rng(3)
+    rows = sorted(set([0, 255, 256, 257, 4096, 4198, 4199] + rng.integers(0, 4200, 12).tolist()))
+    check_rows(case, idx, vals, out, lse, rows)
+    if all_equal:
+        idn = to_np(idx)
+        for t in rows:
+            n = min(cfg.top_k, t + 1)
+            assert np.array_equal(np.sort(idn[t, :n]), np.arange(n)), t
+
+
 def test_topk_ties_match_oracle_exactly():
     # integer-valued scores with many ties: the tie rule (smaller position) fixes the set
     cfg = W.custom([3], [3000], top_k=100)
