@@ -93,6 +93,8 @@ def work_model(cfg):
     sfa_bytes = TQ * cfg.h * D * es_kv + sel * D * es_kv + idx_b + TQ * cfg.h * (cfg.d_c * es_o + 4)
     return {
         "indexer": {"bytes": indexer_bytes, "flops": 2 * cfg.h_idx * cfg.d_idx * pairs},
+        # Top-K reads each causal score once and writes the indices
+        "topk": {"bytes": pairs * 4 + idx_b, "flops": 0},
         "sfa": {"bytes": sfa_bytes, "flops": 2 * cfg.h * (D + cfg.d_c) * sel},
         "pairs": pairs, "selected": sel,
     }
@@ -343,6 +345,17 @@ def main():
     kernels = {k: {"launches": len(v), "ms_mean": statistics.mean(v),
                    "share": sum(v) / sum(sum(x) for x in per_kernel.values())}
                for k, v in per_kernel.items()}
+    # every kernel against its own bound: bytes for decode and Top-K, flops otherwise
+    for k, v in kernels.items():
+        st = KERNEL_STAGE.get(k)
+        if st not in model:
+            continue
+        if decode_like or st == "topk":
+            ach = model[st]["bytes"] / (v["ms_mean"] / 1e3) / 1e9
+            v.update(achieved=ach, unit="GB/s", frac=ach / peaks["hbm_gbs"])
+        else:
+            ach = model[st]["flops"] / (v["ms_mean"] / 1e3) / 1e12
+            v.update(achieved=ach, unit="TFLOP/s", frac=ach / peaks["bf16_tflops"])
 
     # end to end through the public API: per-step inputs from pinned host memory, result back
     e2e = None
