@@ -360,8 +360,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     int nseg = 0, since = 0;
     Cursor<QB> cur;
     cur.locate(tabs, g0);
+    // FP8: the key scale of this thread's key, loaded one item ahead (clamped to a real key
+    // of the block) so that its latency hides behind the previous item
+    auto key_scale = [&](const Cursor<QB>& c) -> float {
+      const int s = min(c.j * C::BM + quarter * 32 + lane, c.pos + c.nrow - 1);
+      return __ldg(p.k_scale + c.k0 + s);
+    };
+    float ksc = FP8 ? key_scale(cur) : 1.f;
+    float wreg[QB == 1 ? C::HI : 1];  // QB = 1: the row's head weights, in registers
     for (int g = g0, it = 0; g < g1; ++g, ++it) {
       if (g > g0) cur.advance(tabs);
+      float ksc_next = 1.f;
+      if (FP8 && g + 1 < g1) {
+        Cursor<QB> nx = cur;
+        nx.advance(tabs);
+        ksc_next = key_scale(nx);
+      }
       if (g == g0 || cur.j == 0) {
         __syncwarp();
 #pragma unroll
@@ -378,6 +392,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           wq[rr * C::HI + lane + 32] = w1;
         }
         __syncwarp();
+        if (QB == 1)
+#pragma unroll
+          for (int jj = 0; jj < C::HI; ++jj) wreg[jj] = wq[jj];
       }
       const int acc = it & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it >> 1) & 1, abort_flag, p.status,
@@ -386,19 +403,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS +
                              rgrp * C::RPW * C::HI;
+      // Σ_j w_j · ReLU(z_j) as four interleaved partial sums (a short dependency chain)
       float sum[C::RPW];
 #pragma unroll
       for (int rr = 0; rr < C::RPW; ++rr) {
-        uint32_t r[32];
-        sum[rr] = 0.f;
-        tmem_ld32(taddr + rr * C::HI, r);
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          sum[rr] = fmaf(wq[rr * C::HI + jj], fmaxf(__uint_as_float(r[jj]), 0.f), sum[rr]);
-        tmem_ld32(taddr + rr * C::HI + 32, r);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t r[32];
+          tmem_ld32(taddr + rr * C::HI + 32 * h2, r);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          sum[rr] = fmaf(wq[rr * C::HI + 32 + jj], fmaxf(__uint_as_float(r[jj]), 0.f), sum[rr]);
+          for (int jj = 0; jj < 32; ++jj) {
+            const float wj = QB == 1 ? wreg[32 * h2 + jj] : wq[rr * C::HI + 32 * h2 + jj];
+            part[jj & 3] = fmaf(wj, fmaxf(__uint_as_float(r[jj]), 0.f), part[jj & 3]);
+          }
+        }
+        sum[rr] = (part[0] + part[1]) + (part[2] + part[3]);
       }
       tc_fence_before();
       __syncwarp();
@@ -406,18 +426,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       const int s = cur.j * C::BM + quarter * 32 + lane;
 #pragma unroll
       for (int rr = 0; rr < C::RPW; ++rr) {
-        const int r = rgrp * C::RPW + rr;
-        if (r < cur.nrow && s <= cur.pos + r) {
-          float v = sum[rr];
-          if (FP8) v *= __ldg(p.k_scale + cur.k0 + s);
-          p.scores[(int64_t)(cur.t + r) * p.ld + s] = v;
-          if (p.hist) {
+        const int r = rgrp * C::RPW + rr;  // the same in the whole warp
+        const bool valid = r < cur.nrow && s <= cur.pos + r;
+        float v = sum[rr];
+        if (FP8) v *= ksc;
+        if (valid) p.scores[(int64_t)(cur.t + r) * p.ld + s] = v;
+        if (p.hist) {
+          // scores of neighbouring keys share bins: one shared-memory atomic per bin per warp
+          if (valid) {
             const uint32_t bin = order_key(v) >> 20;
             if (QB == 1) atomicAdd(&hs[bin], 1u);
             else atomicAdd(&hs[(r * kHistBins + bin) >> 1], 1u << (16 * (bin & 1)));
           }
         }
       }
+      ksc = ksc_next;
       const bool seg_end = g + 1 == g1 || cur.j + 1 == cur.ntiles;
       if (p.hist && (seg_end || (QB > 1 && ++since == kFlushItems))) {
         // add this CTA's counts to the rows' histograms, then start again from zero
