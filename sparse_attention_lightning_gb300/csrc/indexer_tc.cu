@@ -57,9 +57,13 @@ struct Cfg {
   static constexpr int KSTEPS = FP8 ? 4 : 8;       // MMAs per tile (32 B of K each)
   static constexpr int ACC_COLS = N;               // fp32 accumulator columns
   static constexpr int TMEM_COLS = 2 * ACC_COLS;   // double buffered
-  static constexpr int EPI_WARPS = QB == 1 ? 4 : 8;
+  static constexpr int EPI_WARPS = 8;
+  // QB = 1: two groups of four warps take alternate tiles (group g owns accumulator g), so
+  // a tile's epilogue has two MMA periods; QB = 4: one group, two warps per lane quarter
+  static constexpr int GROUPS = QB == 1 ? 2 : 1;
+  static constexpr int GROUP_WARPS = EPI_WARPS / GROUPS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int RPW = QB * 4 / EPI_WARPS;   // query rows per epilogue warp
+  static constexpr int RPW = QB * 4 / GROUP_WARPS;  // query rows per epilogue warp
   // per-row histograms: 32-bit counters for one row, 16-bit ones (flushed before they
   // can overflow) for a block of four
   static constexpr int HIST_BYTES = QB == 1 ? kHistBins * 4 : QB * kHistBins * 2;
@@ -260,7 +264,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     for (int i = 0; i < C::NS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
-      mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], C::EPI_WARPS);
+      mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], C::GROUP_WARPS);
     }
     mbar_init(drain, 1);
     mbar_init(epi_a, EPI_THREADS);
@@ -354,28 +358,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // ---------------- epilogue: TMEM lane quarter warp % 4, rows rgrp * RPW .. ----------------
     const int ew = warp - 2;
     const int quarter = warp & 3;
-    const int rgrp = ew >> 2;        // QB = 4: rows {2 rgrp, 2 rgrp + 1}; QB = 1: row 0
+    const int grp = C::GROUPS == 2 ? ew >> 2 : 0;   // tiles it with it % GROUPS == grp
+    const int rgrp = C::GROUPS == 2 ? 0 : ew >> 2;  // QB = 4: rows {2 rgrp, 2 rgrp + 1}
     const int e = threadIdx.x - 64;  // 0 .. EPI_THREADS - 1
     float* wq = wsm + ew * C::RPW * C::HI;
     int nseg = 0, since = 0;
     Cursor<QB> cur;
     cur.locate(tabs, g0);
-    // FP8: the key scale of this thread's key, loaded one item ahead (clamped to a real key
-    // of the block) so that its latency hides behind the previous item
+    // FP8: the key scale of this thread's key (clamped to a real key of the block)
     auto key_scale = [&](const Cursor<QB>& c) -> float {
       const int s = min(c.j * C::BM + quarter * 32 + lane, c.pos + c.nrow - 1);
       return __ldg(p.k_scale + c.k0 + s);
     };
-    float ksc = FP8 ? key_scale(cur) : 1.f;
     float wreg[QB == 1 ? C::HI : 1];  // QB = 1: the row's head weights, in registers
     for (int g = g0, it = 0; g < g1; ++g, ++it) {
       if (g > g0) cur.advance(tabs);
-      float ksc_next = 1.f;
-      if (FP8 && g + 1 < g1) {
-        Cursor<QB> nx = cur;
-        nx.advance(tabs);
-        ksc_next = key_scale(nx);
-      }
       if (g == g0 || cur.j == 0) {
         __syncwarp();
 #pragma unroll
@@ -396,6 +393,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
           for (int jj = 0; jj < C::HI; ++jj) wreg[jj] = wq[jj];
       }
+      const bool mine = C::GROUPS == 1 || (it & 1) == grp;
+      if (mine) {
+      // issued before the wait for the accumulator, which hides its latency
+      const float ksc = FP8 ? key_scale(cur) : 1.f;
       const int acc = it & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it >> 1) & 1, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT)))
@@ -440,7 +441,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           }
         }
       }
-      ksc = ksc_next;
+      }  // mine
       const bool seg_end = g + 1 == g1 || cur.j + 1 == cur.ntiles;
       if (p.hist && (seg_end || (QB > 1 && ++since == kFlushItems))) {
         // add this CTA's counts to the rows' histograms, then start again from zero
