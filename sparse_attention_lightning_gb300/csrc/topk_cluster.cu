@@ -425,12 +425,12 @@ int topk_cluster_size(int max_k_len) {
   return (max_k_len + 16 * kT - 1) / (16 * kT);
 }
 
-// Decode-like batches: every CTA of a cluster waits for the others, so rows are kept to a few
-// thousand (prefill batches, whose many short rows would leave most CTAs idle, use the
-// segmented kernel).
+// Few rows: when all clusters fit on the GPU at once, spreading a row over up to 8 SMs
+// shortens the (latency-bound) step; beyond one wave the streaming kernel, one CTA per
+// row and several rows per SM, does more work per SM and wins.
 bool topk_cluster_eligible(const TopkArgs& a) {
   return a.hist != nullptr && a.seqs.max_k_len <= kMaxCluster * 16 * kT &&
-         a.seqs.total_q <= 4096;
+         (int64_t)a.seqs.total_q * topk_cluster_size(a.seqs.max_k_len) <= num_sms();
 }
 
 int launch_topk_cluster(const TopkArgs& a, cudaStream_t stream) {

@@ -9,7 +9,8 @@
 //
 // The histogram gives the bin B* that holds the n-th largest key, the count of keys
 // above it and the count in it.  The CTA then reads the row once, 8192 keys at a time
-// (32 consecutive keys per thread): keys above B* ("definite") go straight to the
+// (bulk copies into a double-buffered tile in shared memory, the next tile in flight
+// while this one is processed; 32 consecutive keys per thread): keys above B* ("definite") go straight to the
 // output row at a running offset (block prefix sums keep position order), keys in B*
 // ("candidates") are collected with their positions in shared memory (or, for a row
 // whose histogram says they will not fit, just their positions in the row's slot of the
@@ -19,9 +20,12 @@
 // then the selected candidates ascending, as the other Top-K kernels write them.  No
 // CTA waits for another, so many rows are in flight on every SM.
 #include "dsa_internal.cuh"
+#include "tc_sm100.cuh"
 
 namespace dsa {
 namespace {
+
+using namespace tc;
 
 constexpr int kT = 256;
 constexpr int kW = kT / 32;
@@ -30,6 +34,8 @@ constexpr int kTile = kT * kKPT;       // 8192
 constexpr int kCap = 4096;             // candidates refined from shared memory
 
 struct ShS {
+  float tile[2][kTile];                // the row, two 8192-key tiles at a time
+  uint64_t tbar[2];
   uint32_t warp_a[kW], warp_b[kW];
   uint64_t warp_s[kW];
   uint32_t hist[2048];
@@ -123,7 +129,7 @@ __device__ __forceinline__ uint32_t suffix_above(uint32_t mine, uint32_t* warp_b
   return r;
 }
 
-__global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a, int32_t* spill,
+__global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t* spill,
                                                          int64_t spill_ld) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ShS& S = *reinterpret_cast<ShS*>(smem_raw);
@@ -187,53 +193,86 @@ __global__ void __launch_bounds__(kT, 4) topk_stream_kernel(TopkArgs a, int32_t*
   };
 
   // ---- stream the row: definite positions out, candidates collected ----
+  // tile i of the row into buffer i & 1 (16-byte rounded: the row's leading dimension is a
+  // multiple of 32 scores, so the copy stays inside the row)
+  const int ntile = (n + kTile - 1) / kTile;
+  auto fetch = [&](int i) {
+    const int base = i * kTile;
+    const uint32_t bytes = (uint32_t)((min(kTile, n - base) * 4 + 15) & ~15);
+    mbar_arrive_expect_tx(&S.tbar[i & 1], bytes);
+    bulk_load(S.tile[i & 1], row + base, bytes, &S.tbar[i & 1]);
+  };
+  __shared__ int abort_word;
+  if (tid == 0) {
+    abort_word = 0;
+    mbar_init(&S.tbar[0], 1);
+    mbar_init(&S.tbar[1], 1);
+    fence_barrier_init();
+    fetch(0);
+    if (ntile > 1) fetch(1);
+  }
+  __syncthreads();
   uint32_t def_base = 0, cand_base = 0;
-  for (int base = 0; base < n; base += kTile) {
+  int landed = 0;  // tiles consumed
+  for (int ti = 0; ti < ntile; ++ti) {
+    const int base = ti * kTile;
     const int i0 = base + kKPT * tid;
+    // the same outcome in every thread, so that no thread is left at a barrier
+    const bool ok = mbar_wait(&S.tbar[ti & 1], (ti >> 1) & 1, &abort_word, a.status,
+                              DSA_FLAG_TIMEOUT);
+    if (__syncthreads_or(!ok)) break;
+    landed = ti + 1;
+    const float* tl = S.tile[ti & 1] + kKPT * tid;
     float f[kKPT];
 #pragma unroll
     for (int q = 0; q < kKPT / 4; ++q) {
-      const int i = i0 + 4 * q;
-      if (i + 3 < n) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
-        f[4 * q] = v.x; f[4 * q + 1] = v.y; f[4 * q + 2] = v.z; f[4 * q + 3] = v.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) f[4 * q + e] = i + e < n ? row[i + e] : 0.f;
-      }
+      const float4 v = reinterpret_cast<const float4*>(tl)[q];
+      f[4 * q] = v.x; f[4 * q + 1] = v.y; f[4 * q + 2] = v.z; f[4 * q + 3] = v.w;
     }
     uint32_t dm = 0, cm = 0;
 #pragma unroll
     for (int j = 0; j < kKPT; ++j) {
-      if (i0 + j < n) {
-        const uint32_t b = order_key(f[j]) >> 20;
-        if (b > bstar) dm |= 1u << j;
-        else if (b == bstar) cm |= 1u << j;
-      }
+      const uint32_t bin = order_key(f[j]) >> 20;
+      dm |= (uint32_t)(bin > bstar) << j;
+      cm |= (uint32_t)(bin == bstar) << j;
+    }
+    if (base + kTile > n) {  // the row's last tile: keys past the row do not count
+      const int valid = n - i0;
+      const uint32_t vm = valid >= kKPT ? 0xffffffffu : (valid <= 0 ? 0u : (1u << valid) - 1u);
+      dm &= vm;
+      cm &= vm;
     }
     uint32_t tot;
     const uint32_t pre = scan_pair((uint32_t)__popc(dm) | ((uint32_t)__popc(cm) << 16), S.warp_a,
                                    &tot);
     uint32_t pd = def_base + (pre & 0xffffu), pc = cand_base + (pre >> 16);
-#pragma unroll
-    for (int j = 0; j < kKPT; ++j) {
-      if (dm >> j & 1u) {
-        if (pd < (uint32_t)k) {
-          irow[pd] = i0 + j;
-          if (vrow) vrow[pd] = row[i0 + j];  // read again: the loaded values are not kept
-        }
-        ++pd;
+    // only the (few) set bits: one iteration per selected key
+    for (uint32_t m = dm; m; m &= m - 1u, ++pd) {
+      const int j = __ffs(m) - 1;
+      if (pd < (uint32_t)k) {
+        irow[pd] = i0 + j;
+        if (vrow) vrow[pd] = tl[j];
       }
-      if (cm >> j & 1u) {
-        if (pc < nc) {
-          if (in_smem) S.cand[pc] = make_uint2(order_key(row[i0 + j]), (uint32_t)(i0 + j));
-          else gpos[pc] = i0 + j;
-        }
-        ++pc;
+    }
+    for (uint32_t m = cm; m; m &= m - 1u, ++pc) {
+      const int j = __ffs(m) - 1;
+      if (pc < nc) {
+        if (in_smem) S.cand[pc] = make_uint2(order_key(tl[j]), (uint32_t)(i0 + j));
+        else gpos[pc] = i0 + j;
       }
     }
     def_base += tot & 0xffffu;
     cand_base += tot >> 16;
+    __syncthreads();  // everyone is done with this buffer
+    if (tid == 0 && ti + 2 < ntile) fetch(ti + 2);
+  }
+  if (landed < ntile) {
+    // a copy that never landed (timed out): wait, bounded, for the ones still in flight,
+    // then give up on the row
+    if (tid == 0)
+      for (int i = landed; i < min(ntile, landed + 2); ++i)
+        mbar_wait_drain(&S.tbar[i & 1], (i >> 1) & 1);
+    return;
   }
   if (tid == 0 && (def_base != above || cand_base != nc)) atomicOr(a.status, DSA_FLAG_BAD_SEQS);
   if (!in_smem) __threadfence_block();
