@@ -313,9 +313,9 @@ SfaArgs sfa_args(const dsa_problem* p, const void* q, const void* kv, const int3
 }
 
 int run_sfa(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx, void* out,
-            float* lse, void* ws, void* scratch, cudaStream_t s, bool counters_zeroed = false) {
+            float* lse, void* ws, void* scratch, cudaStream_t s) {
   const SfaArgs sa = sfa_args(p, q, kv, idx, out, lse, ws);
-  if (sfa_tc_eligible(sa)) return launch_sfa_tc(sa, scratch, s, counters_zeroed);
+  if (sfa_tc_eligible(sa)) return launch_sfa_tc(sa, scratch, s);
   return launch_sfa_simt(sa, s);
 }
 
@@ -440,13 +440,9 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
   IndexerScratch sc;
   carve_indexer(p, ws, &sc);
   int32_t* idx = idx_out ? idx_out : sc.idx;
-  // the attention kernel's counters are cleared first, so the three kernels run back to
-  // back (each may start while the one before it finishes)
-  const SfaArgs sa = sfa_args(p, q, kv, idx, out, lse, ws);
-  const bool tc = sfa_tc_eligible(sa);
-  if (tc) DSA_TRY(sfa_tc_clear_counters(sa, sc.sfa, s));
+  // the kernels run back to back: each may start while the one before it finishes
   DSA_TRY(run_fused_indexer(p, q_idx, k_idx, w, q_scale, k_scale, idx, vals_out, ws, s));
-  return run_sfa(p, q, kv, idx, out, lse, ws, sc.sfa, s, tc);
+  return run_sfa(p, q, kv, idx, out, lse, ws, sc.sfa, s);
 }
 
 int dsa_clear_status(void* ws, void* stream) {

@@ -189,13 +189,10 @@ struct SfaArgs {
 };
 int launch_sfa_simt(const SfaArgs& a, cudaStream_t stream);
 
-// tcgen05 SFA (H = 128, d_c = 512, d_rope = 64, bf16) on 2-CTA clusters.
+// tcgen05 SFA (H = 128, d_c = 512, d_rope = 64, bf16) on 2-CTA clusters; with few query
+// rows a second kernel merges the rows cut into pieces.
 bool sfa_tc_eligible(const SfaArgs& a);
 size_t sfa_tc_scratch_bytes(int total_q);
-int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream,
-                  bool counters_zeroed = false);
-// Zero the split-row arrival counters of the tensor-core path ahead of time (so that no
-// memset separates the kernels of a fused call); a no-op without a split.
-int sfa_tc_clear_counters(const SfaArgs& a, void* scratch, cudaStream_t stream);
+int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream);
 
 }  // namespace dsa

@@ -25,7 +25,7 @@
 // operand from there), which leaves shared memory to a 4-stage ring of gathered
 // rows and double send and receive exchange buffers.  TMEM: O (128 x 256 fp32) |
 // Q (144 columns of bf16 pairs) | S (128 x 64 fp32) | P (64 bf16 per head) | 8
-// columns for swapping per-head values between the two halves.
+// columns for passing per-head values between the two softmax groups.
 //
 // Per chunk of 64 selected rows:
 //  * two producer warps (32 rows each): the 16-byte pieces of the CTA's columns
@@ -34,19 +34,23 @@
 //  * MMA thread: S = Q_cols · KV_cols^T (M=128, N=64, K=288; A from TMEM, B
 //    K-major in shared memory), then, once P is ready, O += P · V (M=128, N=256,
 //    K=64; P from TMEM, V read MN-major straight from the gathered tile);
-//  * softmax warps (two warpgroups; a thread per head and half of the chunk's
-//    columns): read their 32 partial logits from TMEM (S is then free for the next
-//    chunk's MMA), scale them to log2 units, round to fp16 and stage them; the last
-//    warp to stage ships the CTA's 16 KB to the peer with one bulk copy.  A chunk is
-//    staged before the previous one is processed whenever its logits are ready, so
-//    the exchange overlaps the softmax.  Processing adds the peer's fp16 partials to
-//    the thread's own (the same sum in both CTAs), takes the chunk max (the two halves
-//    of a head swap theirs through TMEM), keeps a running max (O is rescaled only when
-//    it grows by more than 2^8) and writes its half of P = 2^(x - m) as bf16 into
-//    TMEM, where the P·V MMA reads it as its A operand.
+//  * softmax warps: two groups of four take alternate chunks, so two chunks are in
+//    flight (one group waits for its exchange while the other computes); a thread
+//    holds one head's 64 columns of its group's chunk.  It reads its partial logits
+//    from TMEM (S is then free for the next chunk's MMA), scales them to log2 units,
+//    rounds them to fp16 and stages them; each warp ships its 4 KB block to the peer
+//    with one bulk copy.  Processing adds the peer's fp16 partials to the thread's own
+//    (the same sum in both CTAs), takes the chunk max, moves the running reference
+//    (shared by the two groups through TMEM; it moves only when the max grows by more
+//    than 2^8, and O is then rescaled) and writes P = 2^(x - m) as bf16 into TMEM,
+//    where the P·V MMA reads it as its A operand.
 //
-// Decode rows are split over 2 clusters when there are few queries; the second
-// cluster of a row to finish merges the other's partial (O, max, sum) into its own.
+// Work schedule.  With many query rows, cluster c takes whole rows c, c + clusters, ...
+// With few (decode), the rows' chunk slots (ceil(top_k / 64) per row) are laid end to
+// end and cut into one contiguous, equal share per cluster, so every cluster gathers
+// the same number of chunks; a row cut by share boundaries is attended in pieces, each
+// piece writes its partial (O, max, sum), and a second kernel (sfa_combine_kernel, all
+// SMs) merges each cut row's pieces in piece order.
 // Every wait is bounded (DSA_FLAG_TIMEOUT).
 #include <cuda_fp16.h>
 
@@ -77,26 +81,28 @@ constexpr int kOCol = 0;                      // O: 256 fp32 columns
 constexpr int kQCol = 256;                    // Q: 144 columns (2 bf16 each)
 constexpr int kSCol = 400;                    // S: 64 fp32 columns
 constexpr int kPCol = 464;                    // P: 32 columns (2 bf16 each)
-constexpr int kXCol = 496;                    // 4 columns: the two halves' sums, 2 phases
-constexpr int kMCol = 500;                    // 4 columns: the two halves' chunk maxima, 2 phases
+constexpr int kXCol = 496;                    // 4 columns: the two groups' sums, 2 phases
+constexpr int kMCol = 500;                    // 2 columns: the reference decided at a chunk, by parity
 constexpr float kRescaleLog2 = 8.0f;          // rescale O only when the max grows > 2^8
 static_assert(kMCol + 4 <= kTmemCols, "TMEM layout");
-static_assert(kStages * kKVStage + 2 * kXBytes >= kH * 256 * 4, "merge staging area");
+static_assert(kStages * kKVStage >= kH * 256 * 4, "merge staging area");
 
 struct Params {
   Seqs seqs;
   int top_k;
   float scale_log2;  // softmax scale · log2(e)
-  int nsplit;
+  int pieces;        // 1: equal contiguous shares of chunk slots; 0: whole rows
+  int C;             // chunk slots of a row: max(1, ceil(top_k / 64))
+  int64_t tot;       // total_q * C
+  int nclusters;     // clusters of the attention grid
   int out_f32;
   const __nv_bfloat16* q;
   const int32_t* idx;
   const __nv_bfloat16* kv;
   void* out;
   float* lse;
-  float4* part_o;    // [total_q * nsplit * 2][64][128] float4 (nsplit > 1)
-  float* part_ml;    // [total_q * nsplit * 2][128][2]
-  int* counters;     // [total_q * 2], zero at launch
+  float4* part_o;    // [(total_q + clusters - 1) * 2][64][128] float4 (pieces)
+  float* part_ml;    // [(total_q + clusters - 1) * 2][128][2]
   int32_t* lists;    // [gridDim.x][kMaxTopK]: each CTA's compacted key rows of its unit
   uint32_t* status;
 };
@@ -133,10 +139,43 @@ __device__ __forceinline__ int seq_of_row(const Seqs& s, int t, int lane) {
   return lo;
 }
 
-// The split `sp` of a row with nv selected keys: rows [lo, lo + n) of its list.
-__device__ __forceinline__ void unit_range(int nv, int sp, int nsplit, int& lo, int& n) {
-  lo = (int)((int64_t)nv * sp / nsplit);
-  n = (int)((int64_t)nv * (sp + 1) / nsplit) - lo;
+// A piece of work: chunk slots [a, b) of query row t, i.e. idx[t, 64a : min(64b, top_k)).
+struct Piece {
+  int t, a, b;
+};
+
+// Share of cluster c in the laid-out chunk slots: [B(c), B(c + 1)), B(c) = floor(c·tot/ncl).
+__device__ __forceinline__ int64_t share_begin(const Params& p, int c, int ncl) {
+  return (int64_t)c * p.tot / ncl;
+}
+// The cluster whose share holds chunk slot x: the last c with B(c) <= x.
+__device__ __forceinline__ int share_of(const Params& p, int64_t x, int ncl) {
+  return (int)(((x + 1) * ncl - 1) / p.tot);
+}
+
+// The k-th piece of cluster cid's work; false past its end.
+__device__ __forceinline__ bool piece_at(const Params& p, int cid, int ncl, int k, Piece& pc) {
+  if (!p.pieces) {
+    pc.t = cid + k * ncl;
+    pc.a = 0;
+    pc.b = p.C;
+    return pc.t < p.seqs.total_q;
+  }
+  const int64_t x0 = share_begin(p, cid, ncl), x1 = share_begin(p, cid + 1, ncl);
+  const int t = (int)(x0 / p.C) + k;
+  const int64_t r0 = (int64_t)t * p.C;
+  if (r0 >= x1) return false;
+  pc.t = t;
+  pc.a = k == 0 ? (int)(x0 - r0) : 0;
+  pc.b = (int)min((int64_t)p.C, x1 - r0);
+  return true;
+}
+
+// The clusters [cf, cf + np) whose shares hold row t's chunk slots (np = 1: not cut).
+__device__ __forceinline__ void row_pieces(const Params& p, int t, int ncl, int& cf, int& np) {
+  if (!p.pieces) { cf = -1; np = 1; return; }
+  cf = share_of(p, (int64_t)t * p.C, ncl);
+  np = share_of(p, (int64_t)(t + 1) * p.C - 1, ncl) - cf + 1;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -150,49 +189,42 @@ sfa_tc_kernel(Params p) {
   int32_t* list = p.lists + (int64_t)blockIdx.x * kMaxTopK;  // global: written and read here
   uint64_t* kv_full = bars;              // [kStages] 64 producer lanes (cp.async completion)
   uint64_t* kv_empty = bars + 4;         // [kStages]
-  uint64_t* s_full = bars + 8;
-  uint64_t* s_empty = bars + 9;          // 8 softmax warps have read S
+  uint64_t* s_empty = bars + 9;          // the 4 warps of the chunk's group have read S
   uint64_t* q_full = bars + 10;          // 8 softmax warps have stored Q
-  uint64_t* p_full = bars + 11;
-  uint64_t* p_empty = bars + 12;
-  uint64_t* pv_done = bars + 13;
-  uint64_t* x_full = bars + 14;          // [2] the peer's st.async bytes land here
-  uint64_t* x_empty = bars + 16;         // [2] the peer's 8 softmax warps: buffer read
+  uint64_t* p_full = bars + 11;          // the 4 warps of the chunk's group have stored P
+  uint64_t* x_full = bars + 14;          // [2] the peer's bulk copies land here (16 KB)
+  uint64_t* x_empty = bars + 16;         // [2] the peer's 4 warps of the group: buffer read
   uint64_t* meta_full = bars + 18;
   uint64_t* meta_empty = bars + 19;
-  uint64_t* drain = bars + 20;           // [2]: MMA drain, merge copy
-  uint64_t* sync_a = bars + 22;          // 256 softmax threads: partials written
-  uint64_t* sync_b = bars + 23;          // the arrival count has been taken
-  uint64_t* hsync = bars + 24;           // the 8 softmax warps: per-head halves exchanged
+  uint64_t* drain = bars + 20;           // MMA drain
+  uint64_t* hsync = bars + 24;           // the 8 softmax warps: the two groups' sums exchanged
   volatile int* meta_nv = reinterpret_cast<volatile int*>(bars + 25);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 27);
-  int* s_last = reinterpret_cast<int*>(bars + 28);
-  uint64_t* pairb = bars + 29;           // [4] the two softmax warps of a lane quarter
-  uint32_t* x_count = reinterpret_cast<uint32_t*>(bars + 33);  // [2] staging arrivals, ever
+  uint64_t* dec = bars + 29;             // [2] by chunk parity: its group published the reference
+  // Per chunk parity (a softmax group waits only for its own chunks' phases, so that no
+  // parity wait can run ahead of the barrier):
+  uint64_t* s_full = bars + 31;          // [2] the chunk's logit MMA is complete
+  uint64_t* pv_done = bars + 33;         // [2] the chunk's P·V MMA is complete (P, O free)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int gbase = rank ? 256 : 0;            // first kv column gathered = first output column
   const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-  const int nunits = p.seqs.total_q * p.nsplit;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&kv_full[i], 64); mbar_init(&kv_empty[i], 1); }
-    mbar_init(s_full, 1); mbar_init(s_empty, 8);
+    mbar_init(s_empty, 4);
     mbar_init(q_full, 8);
-    mbar_init(p_full, 8); mbar_init(p_empty, 1); mbar_init(pv_done, 1);
+    mbar_init(p_full, 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 8);
-      x_count[i] = 0;
+      mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 4);
+      mbar_init(&dec[i], 4);
+      mbar_init(&s_full[i], 1); mbar_init(&pv_done[i], 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&pairb[i], 2);
     mbar_init(meta_full, 1); mbar_init(meta_empty, 10);
     mbar_init(drain, 1);
-    mbar_init(drain + 1, 1);
-    mbar_init(sync_a, 256);
-    mbar_init(sync_b, 1);
     mbar_init(hsync, 8);
     *abort_flag = 0;
     fence_barrier_init();
@@ -202,14 +234,16 @@ sfa_tc_kernel(Params p) {
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (p.pieces && threadIdx.x == 0) griddep_launch();  // the merge kernel may be scheduled (it waits)
 
   if (warp == 0 || warp == 10) {
     // -------- producer warps: index compaction (warp 0), gathers (32 rows each) --------
     const int pw = warp == 0 ? 0 : 1;
     int gc = 0;
     bool stop = false;
-    for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
-      const int t = u / p.nsplit, sp = u - t * p.nsplit;
+    Piece pc;
+    for (int ui = 0; !stop && piece_at(p, cluster_id, nclusters, ui, pc); ++ui) {
+      const int t = pc.t;
       int nv;
       if (pw == 0) {
         const int b = seq_of_row(p.seqs, t, lane);
@@ -223,18 +257,20 @@ sfa_tc_kernel(Params p) {
         const int pos = (k1 - k0) - (q1 - q0) + (t - q0);
         const bool ok = t >= q0 && t < q1 && q1 - q0 <= k1 - k0 && k0 >= 0 &&
                         k1 <= p.seqs.total_k && k1 - k0 <= p.seqs.max_k_len;
-        // valid entries of idx[t, :] in slot order -> list (absolute key rows).  Each lane
-        // owns a contiguous run of up to 64 slots, loaded all at once (independent loads).
-        // The Top-K kernel that writes idx may still be running: wait for it here, after
-        // the work that does not depend on it.
+        // valid entries of the piece's slots of idx[t, :], in slot order -> list (absolute
+        // key rows).  Each lane owns a contiguous run of up to 64 slots, loaded all at once
+        // (independent loads).  The Top-K kernel that writes idx may still be running: wait
+        // for it here, after the work that does not depend on it.
         griddep_wait();
-        const int32_t* irow = p.idx + (int64_t)t * p.top_k;
-        const int seg = (p.top_k + 31) / 32;
+        const int slo = pc.a * kNC, shi = min(pc.b * kNC, p.top_k);
+        const int32_t* irow = p.idx + (int64_t)t * p.top_k + slo;
+        const int len = max(shi - slo, 0);
+        const int seg = (len + 31) / 32;
         const int s0 = lane * seg;
         int v[kMaxTopK / 32];
 #pragma unroll
         for (int j = 0; j < kMaxTopK / 32; ++j)
-          v[j] = (ok && j < seg && s0 + j < p.top_k) ? __ldg(irow + s0 + j) : -1;
+          v[j] = (ok && j < seg && s0 + j < len) ? __ldg(irow + s0 + j) : -1;
         int cnt = 0;
         bool bad = false;
 #pragma unroll
@@ -243,7 +279,7 @@ sfa_tc_kernel(Params p) {
           bad |= !valid && v[j] != -1;
           cnt += valid;
         }
-        if (bad && sp == 0 && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
+        if (bad && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
         int before = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -267,8 +303,7 @@ sfa_tc_kernel(Params p) {
           break;
         nv = *meta_nv;
       }
-      int lo, n;
-      unit_range(nv, sp, p.nsplit, lo, n);
+      const int n = nv;
       const int nch = (n + kNC - 1) / kNC;
       // lane = (row sub-index r4 = lane / 8, 16-byte piece lane % 8) for whole atoms;
       // (r8 = lane / 4, piece lane % 4) for CTA 0's half atom (columns 256..287)
@@ -283,12 +318,12 @@ sfa_tc_kernel(Params p) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const int jj = c * kNC + rbase + g * 4 + r4;
-          rowid[g] = list[lo + (jj < n ? jj : 0)];
+          rowid[g] = list[jj < n ? jj : 0];
         }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int jj = c * kNC + rbase + g * 8 + r8;
-          rowh[g] = list[lo + (jj < n ? jj : 0)];
+          rowh[g] = list[jj < n ? jj : 0];
         }
       };
       if (nch > 0) load_rows(0);
@@ -337,14 +372,12 @@ sfa_tc_kernel(Params p) {
       const int koff = rank ? 2 : 0;  // CTA 1's logit columns start half-way into atom 0
       int gc = 0;
       bool stop = false;
-      for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
+      Piece pc;
+      for (int ui = 0; !stop && piece_at(p, cluster_id, nclusters, ui, pc); ++ui) {
         if (!mbar_wait(meta_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         const int nv = *meta_nv;
         mbar_arrive(meta_empty);
-        const int sp = u % p.nsplit;
-        int lo, n;
-        unit_range(nv, sp, p.nsplit, lo, n);
-        const int nch = (n + kNC - 1) / kNC;
+        const int nch = (nv + kNC - 1) / kNC;
         if (!mbar_wait(q_full, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT)) break;
         tc_fence_after();
         if (nch == 0) continue;
@@ -372,7 +405,7 @@ sfa_tc_kernel(Params p) {
                 const uint64_t bd = bd0 + (uint64_t)(((k >> 2) * (kNC * 128) + (k & 3) * 32) >> 4);
                 mma_bf16_ts(tmem + kSCol, tmem + kQCol + i * 8, bd, idesc_s, i ? 1u : 0u);
               }
-              mma_commit(s_full);
+              mma_commit(&s_full[g & 1]);
               ++si;
               did = true;
             }
@@ -389,8 +422,7 @@ sfa_tc_kernel(Params p) {
                             (pi > 0 || kk > 0) ? 1u : 0u);
               }
               mma_commit(&kv_empty[g % kStages]);
-              mma_commit(p_empty);
-              mma_commit(pv_done);
+              mma_commit(&pv_done[g & 1]);
               ++pi;
               did = true;
             }
@@ -413,86 +445,69 @@ sfa_tc_kernel(Params p) {
       mbar_wait_drain(drain, 0);
     }
   } else {
-    // ---------------- softmax / epilogue: 2 warpgroups; thread = (head, half of the chunk) ----
+    // ------- softmax / epilogue: two groups of 4 warps take alternate chunks (group g takes
+    // the chunks with global index = g mod 2); thread = (head, all 64 columns of a chunk) -------
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;        // warps 2..5: columns 0..31, warps 6..9: 32..63
+    const int grp = (warp - 2) >> 2;          // warps 2..5: even chunks, 6..9: odd chunks
     const int h = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t xs_peer = mapa(smem_u32(xs), peer);  // our partial goes there
+    const uint32_t xs_peer = mapa(smem_u32(xs), peer);  // our partials go there
     const uint32_t x_full_peer = mapa(smem_u32(x_full), peer);
     const uint32_t x_empty_peer = mapa(smem_u32(x_empty), peer);
-    const bool leader = threadIdx.x == 64;
+    const bool gleader = quarter == 2 && lane == 0;     // first warp of the group (2 or 6)
     int gc = 0, nsync = 0;
     bool stop = false;
-    // Stage chunk g: read this thread's 32 partial logits from TMEM (then S is free for
-    // the next logit MMA), scale them to log2 units, round to fp16 and write them to the
-    // staging buffer ([8][128] x 8 halves: both halves of every head).  The last of the 8
-    // warps to stage ships the 16 KB to the peer with one bulk copy that completes on the
-    // peer's x_full.  The link between the two SMs moves ~12 B per clock: fp16 halves the
-    // time fp32 would take and keeps 2^-11 relative precision, below the bf16 rounding P
-    // gets anyway; one bulk copy (rather than per-thread remote stores, which update the
-    // peer's mbarrier every 16 bytes) leaves the peer's tensor core undisturbed.
-    auto stage = [&](int g, uint32_t (&own)[16]) -> bool {
-      const int xb = g & 1;
-      const uint32_t xph = (g >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort_flag, p.status,
+    // Stage chunk g (this group's): read the thread's 64 partial logits from TMEM (then S
+    // is free for the next logit MMA), scale them to log2 units, round to fp16 and keep
+    // them; each warp writes its 4 KB block (32 heads x 64 columns) of the group's send
+    // buffer and ships it to the same place in the peer's receive buffer with one bulk
+    // copy, which completes on the peer's x_full (16 KB a chunk).  The link between the
+    // two SMs moves ~12 B per clock: fp16 halves the time fp32 would take and keeps 2^-11
+    // relative precision, below the bf16 rounding P gets anyway; bulk copies (rather than
+    // per-thread remote stores, which update the peer's mbarrier every 16 bytes) leave the
+    // peer's tensor core undisturbed.
+    auto stage = [&](int g, uint32_t (&own)[32]) -> bool {
+      const uint32_t xph = (g >> 1) & 1;  // parity of the use count of buffer grp
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], xph, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT))) return false;
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(lane_base + kSCol + 32 * half, r);
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + kSCol + 32 * hb, r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float a = __uint_as_float(r[2 * e]) * p.scale_log2;
+          const float b = __uint_as_float(r[2 * e + 1]) * p.scale_log2;
+          const __half2 h2 = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f),
+                                               fminf(fmaxf(b, -65504.f), 65504.f));
+          own[16 * hb + e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty);
       // our x_full will take this chunk's bytes from the peer
-      if (leader) mbar_arrive_expect_tx(&x_full[xb], kXBytes);
+      if (gleader) mbar_arrive_expect_tx(&x_full[grp], kXBytes);
       // the peer has read what we sent two chunks ago, so our copy of it is complete
-      if (!__all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xph ^ 1, abort_flag, p.status,
+      if (!__all_sync(0xffffffffu, mbar_wait(&x_empty[grp], xph ^ 1, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT))) return false;
-      uint4* xout = xsend + xb * (kXBytes / 16);
+      uint4* xout = xsend + grp * (kXBytes / 16) + quarter * 256;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = __uint_as_float(r[8 * q + 2 * e]) * p.scale_log2;
-          const float b = __uint_as_float(r[8 * q + 2 * e + 1]) * p.scale_log2;
-          const __half2 h2 = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f),
-                                               fminf(fmaxf(b, -65504.f), 65504.f));
-          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          own[4 * q + e] = w[e];
-        }
-        xout[(4 * half + q) * kH + h] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
+      for (int q = 0; q < 8; ++q)
+        xout[q * 32 + lane] = make_uint4(own[4 * q], own[4 * q + 1], own[4 * q + 2], own[4 * q + 3]);
       fence_proxy_async_smem();  // our generic writes, seen by the bulk copy
       __syncwarp();
-      if (lane == 0) {
-        uint32_t before;
-        asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
-                     : "=r"(before) : "r"(smem_u32(&x_count[xb])) : "memory");
-        if ((before & 7u) == 7u)
-          bulk_s2peer(xs_peer + (uint32_t)(xb * kXBytes), xout, kXBytes,
-                      x_full_peer + (uint32_t)(xb * 8));
-      }
+      if (lane == 0)
+        bulk_s2peer(xs_peer + (uint32_t)(grp * kXBytes + quarter * 4096), xout, 4096,
+                    x_full_peer + (uint32_t)(grp * 8));
       return true;
     };
-    // the other half's chunk maximum of head h (the warp pair of this lane quarter)
-    auto pair_max = [&](float v, int g) -> float {
-      const uint32_t col = lane_base + kMCol + 2 * (g & 1);
-      tmem_st1(col + half, __float_as_uint(v));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pairb[quarter]);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&pairb[quarter], g & 1, abort_flag,
-                                                        p.status, DSA_FLAG_TIMEOUT));
-      if (!ok) { stop = true; return v; }
-      tc_fence_after();
-      return fmaxf(v, __uint_as_float(tmem_ld1(col + (1 - half))));
-    };
-    // combine a per-head value with the other half's: both halves' warps reach the same
+    // combine a per-head value with the other group's: both groups' warps reach the same
     // TMEM lanes, so the value goes through a TMEM column (bounded 8-warp exchange)
     auto exchange = [&](float v) -> float {
       const uint32_t col = lane_base + kXCol + 2 * (nsync & 1);
-      tmem_st1(col + half, __float_as_uint(v));
+      tmem_st1(col + grp, __float_as_uint(v));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(hsync);
@@ -501,15 +516,27 @@ sfa_tc_kernel(Params p) {
       ++nsync;
       if (!ok) { stop = true; return 0.f; }
       tc_fence_after();
-      return __uint_as_float(tmem_ld1(col + (1 - half)));
+      return __uint_as_float(tmem_ld1(col + (1 - grp)));
     };
-    for (int u = cluster_id, ui = 0; u < nunits && !stop; u += nclusters, ++ui) {
-      const int t = u / p.nsplit, sp = u - t * p.nsplit;
+    // the reference max decided at chunk g (by the group that owns it): TMEM column
+    // kMCol + (g & 1), published on dec[g & 1]
+    auto decided = [&](int g) -> float {
+      if (!__all_sync(0xffffffffu, mbar_wait(&dec[g & 1], (g >> 1) & 1, abort_flag, p.status,
+                                             DSA_FLAG_TIMEOUT))) { stop = true; return 0.f; }
+      tc_fence_after();
+      return __uint_as_float(tmem_ld1(lane_base + kMCol + (g & 1)));
+    };
+    Piece pc;
+    for (int ui = 0; !stop && piece_at(p, cluster_id, nclusters, ui, pc); ++ui) {
+      const int t = pc.t;
+      int cf, np;
+      row_pieces(p, t, nclusters, cf, np);
       // this thread's 72 query columns (144 bf16) -> TMEM, the logit MMA's A operand.
-      // The previous unit's logit MMAs are complete: this thread has read all their S.
+      // The previous piece's logit MMAs are complete: both groups have passed the sum
+      // exchange that ends it, after all of its chunks were staged.
       {
         const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + ((int64_t)t * kH + h) * kD + (rank ? kQK : 0) + 144 * half);
+            p.q + ((int64_t)t * kH + h) * kD + (rank ? kQK : 0) + 144 * grp);
         uint4 qv[18];
 #pragma unroll
         for (int i = 0; i < 18; ++i) qv[i] = __ldg(src + i);
@@ -518,16 +545,16 @@ sfa_tc_kernel(Params p) {
         for (int i = 0; i < 8; ++i) {
           w[4 * i] = qv[i].x; w[4 * i + 1] = qv[i].y; w[4 * i + 2] = qv[i].z; w[4 * i + 3] = qv[i].w;
         }
-        tmem_st32(lane_base + kQCol + 72 * half, w);
+        tmem_st32(lane_base + kQCol + 72 * grp, w);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           w[4 * i] = qv[8 + i].x; w[4 * i + 1] = qv[8 + i].y;
           w[4 * i + 2] = qv[8 + i].z; w[4 * i + 3] = qv[8 + i].w;
         }
-        tmem_st32(lane_base + kQCol + 72 * half + 32, w);
+        tmem_st32(lane_base + kQCol + 72 * grp + 32, w);
         const uint32_t w8[8] = {qv[16].x, qv[16].y, qv[16].z, qv[16].w,
                                 qv[17].x, qv[17].y, qv[17].z, qv[17].w};
-        tmem_st8(lane_base + kQCol + 72 * half + 64, w8);
+        tmem_st8(lane_base + kQCol + 72 * grp + 64, w8);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full);
@@ -537,64 +564,65 @@ sfa_tc_kernel(Params p) {
       const int nv = *meta_nv;
       __syncwarp();
       if (lane == 0) mbar_arrive(meta_empty);
-      int lo, n;
-      unit_range(nv, sp, p.nsplit, lo, n);
+      const int n = nv;
       const int nch = (n + kNC - 1) / kNC;
-      float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the sum
+      // m_mine: the reference this group's share l of the sum is relative to
+      float m_mine = -INFINITY, l = 0.f;
       const int g0 = gc;
-      uint32_t cur[16], nxt[16];  // this thread's staged fp16 partials (32 columns)
-      if (nch > 0 && !stage(g0, cur)) break;
-      for (int c = 0; c < nch; ++c, ++gc) {
-        // stage the next chunk first when its logits are already there, so its exchange is
-        // in flight while this one is processed; otherwise process this one first
-        bool early = false;
-        if (c + 1 < nch) {
-          early = __all_sync(0xffffffffu, mbar_test(smem_u32(s_full), (gc + 1) & 1));
-          if (early && !stage(gc + 1, nxt)) { stop = true; break; }
-        }
+      for (int c = (g0 & 1) == grp ? 0 : 1; c < nch; c += 2) {
+        const int g = g0 + c;
+        uint32_t own[32];  // this chunk's fp16 partials of our CTA (64 columns)
+        if (!stage(g, own)) { stop = true; break; }
         const int rows_in = min(kNC, n - c * kNC);
-        const int xb = gc & 1;               // exchange buffer
-        const uint32_t xph = (gc >> 1) & 1;  // parity of its use count
-        if (!__all_sync(0xffffffffu, mbar_wait(&x_full[xb], xph, abort_flag, p.status,
+        if (!__all_sync(0xffffffffu, mbar_wait(&x_full[grp], (g >> 1) & 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) {
           stop = true; break;
         }
-        // logits of this thread's 32 columns = its CTA's fp16 partial + the peer's (fp16 + fp16
-        // is the same sum in both CTAs, so both take the same softmax decisions)
-        const uint4* oth = xs + xb * (kXBytes / 16);
-        float s[32];
+        // logits = our CTA's fp16 partial + the peer's (fp16 + fp16 is the same sum in both
+        // CTAs, so both take the same softmax decisions)
+        const uint4* oth = xs + grp * (kXBytes / 16) + quarter * 256;
+        float s[64];
         float m_c = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 b4 = oth[(4 * half + q) * kH + h];
+        for (int q = 0; q < 8; ++q) {
+          const uint4 b4 = oth[q * 32 + lane];
           const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&cur[4 * q + e]));
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&own[4 * q + e]));
             const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
             const int i = 8 * q + 2 * e;
-            s[i] = 32 * half + i < rows_in ? fa.x + fb.x : -INFINITY;
-            s[i + 1] = 32 * half + i + 1 < rows_in ? fa.y + fb.y : -INFINITY;
+            s[i] = i < rows_in ? fa.x + fb.x : -INFINITY;
+            s[i + 1] = i + 1 < rows_in ? fa.y + fb.y : -INFINITY;
             m_c = fmaxf(m_c, fmaxf(s[i], s[i + 1]));
           }
         }
         __syncwarp();
-        // the reads above fed m_c: the peer may refill the buffer
-        if (lane == 0) mbar_arrive_remote_relaxed(x_empty_peer + (uint32_t)(xb * 8));
-        m_c = pair_max(m_c, gc);  // the same chunk maximum in both halves
+        // the reads above are done: the peer may refill its send into this buffer
+        if (lane == 0) mbar_arrive_remote_relaxed(x_empty_peer + (uint32_t)(grp * 8));
+        // running reference, shared by the two groups: it moves only when the max grows by
+        // more than 2^8; O (and the other group's share of the sum) follow it lazily
+        const float m_prev = c > 0 ? decided(g - 1) : -INFINITY;
         if (stop) break;
-        // running max: move the reference only when it grows by more than 2^8
-        const bool grow = m_c > m_ref + kRescaleLog2;
-        const float m_new = grow ? m_c : m_ref;
-        const float factor = grow ? ex2(m_ref - m_new) : 1.f;
-        l *= factor;
+        const bool grow = m_c > m_prev + kRescaleLog2;
+        const float m_new = grow ? m_c : m_prev;
+        tmem_st1(lane_base + kMCol + (g & 1), __float_as_uint(m_new));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dec[grp]);
+        if (l > 0.f && m_new > m_mine) l *= ex2(m_mine - m_new);
+        m_mine = m_new;
         if (__any_sync(0xffffffffu, grow && c > 0)) {
-          if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status,
-                                                 DSA_FLAG_TIMEOUT))) { stop = true; break; }
+          // O holds the chunks before g at reference m_prev: rescale it once P·V(g - 1) is in
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1,
+                                                 abort_flag, p.status, DSA_FLAG_TIMEOUT))) {
+            stop = true; break;
+          }
           tc_fence_after();
-          for (int b = 0; b < 4; ++b) {  // this half's 128 output columns
+          const float factor = grow ? ex2(m_prev - m_new) : 1.f;
+          for (int b = 0; b < 8; ++b) {  // the CTA's 256 output columns of head h
             uint32_t r[32];
-            const uint32_t ta = lane_base + kOCol + 128 * half + 32 * b;
+            const uint32_t ta = lane_base + kOCol + 32 * b;
             tmem_ld32(ta, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * factor);
@@ -602,42 +630,46 @@ sfa_tc_kernel(Params p) {
           }
           tc_fence_before();
         }
-        m_ref = m_new;
-        uint32_t pk[16];
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = s[2 * i];
-          const float x1 = s[2 * i + 1];
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(x0 - m_ref), ex2(x1 - m_ref));
+        for (int i = 0; i < 32; ++i) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2(s[2 * i] - m_new), ex2(s[2 * i + 1] - m_new));
           const float2 f2 = __bfloat1622float2(b2);
           l += f2.x + f2.y;
           pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(p_empty, (gc & 1) ^ 1, abort_flag, p.status,
-                                               DSA_FLAG_TIMEOUT))) { stop = true; break; }
+        // P·V(g - 1) has read P (for g = 0 the wait passes: its barrier has no phase yet)
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1,
+                                               abort_flag, p.status, DSA_FLAG_TIMEOUT))) {
+          stop = true; break;
+        }
         tc_fence_after();
-        tmem_st16(lane_base + kPCol + 16 * half, pk);
+        tmem_st32(lane_base + kPCol, pk);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
-        if (c + 1 < nch && !early && !stage(gc + 1, nxt)) { stop = true; break; }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
       }
       if (stop) break;
+      gc = g0 + nch;
 
-      // ---- epilogue of the unit ----
+      // ---- epilogue of the piece ----
       const bool have = nch > 0;
+      float m_ref = -INFINITY;
       if (have) {
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (gc - 1) & 1, abort_flag, p.status,
-                                               DSA_FLAG_TIMEOUT))) break;
+        const int gl = gc - 1;  // the piece's last chunk decided the final reference
+        m_ref = (gl & 1) == grp ? m_mine : decided(gl);
+        if (stop) break;
+        if (l > 0.f && m_ref > m_mine) l *= ex2(m_mine - m_ref);
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[gl & 1], (gl >> 1) & 1, abort_flag,
+                                               p.status, DSA_FLAG_TIMEOUT))) break;
         tc_fence_after();
       }
-      const float lo_sum = exchange(l);  // the other half's share
+      const float lo_sum = exchange(l);  // the other group's share
       if (stop) break;
-      const float ltot = half == 0 ? l + lo_sum : lo_sum + l;  // same order in both halves
+      const float ltot = grp == 0 ? l + lo_sum : lo_sum + l;  // same order in both groups
+      const int half = grp;
       const int ocol = 128 * half;     // this thread's 128 output columns (of the CTA's 256)
-      if (p.nsplit == 1) {
+      if (np == 1) {
         const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
         uint8_t* orow = static_cast<uint8_t*>(p.out) +
                         (((int64_t)t * kH + h) * kDC + gbase + ocol) * (p.out_f32 ? 4 : 2);
@@ -672,8 +704,8 @@ sfa_tc_kernel(Params p) {
           p.lse[(int64_t)t * kH + h] =
               ltot > 0.f ? (m_ref + log2f(ltot)) * 0.69314718055994531f : -INFINITY;
       } else {
-        // split of a row: publish (O, m, l); the second split of the row to finish merges
-        const int64_t slot = ((int64_t)t * p.nsplit + sp) * 2 + rank;
+        // a piece of a cut row: its partial (O, m, l), merged by sfa_combine_kernel
+        const int64_t slot = (int64_t)(cluster_id + t) * 2 + rank;
         float4* po = p.part_o + slot * (64 * kH);
         for (int b = 0; b < 4; ++b) {
           uint32_t r[32];
@@ -691,85 +723,6 @@ sfa_tc_kernel(Params p) {
           p.part_ml[(slot * kH + h) * 2] = m_ref;
           p.part_ml[(slot * kH + h) * 2 + 1] = ltot;
         }
-        // all 256 partial rows are out before the arrival count moves (bounded waits)
-        __threadfence();
-        mbar_arrive(sync_a);
-        if (leader) {
-          const bool okw = mbar_wait(sync_a, ui & 1, abort_flag, p.status, DSA_FLAG_TIMEOUT);
-          *s_last = okw && atomicAdd(p.counters + t * 2 + rank, 1) == p.nsplit - 1;
-          mbar_arrive(sync_b);
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(sync_b, ui & 1, abort_flag, p.status,
-                                               DSA_FLAG_TIMEOUT))) break;
-        if (*s_last) {
-          // The other split's (O, m, l) of this column half: one bulk copy of its
-          // 128 KB into the (now idle) query/KV area, then each thread merges.
-          __threadfence();
-          const int64_t other = ((int64_t)t * p.nsplit + (1 - sp)) * 2 + rank;
-          float4* po2 = reinterpret_cast<float4*>(kvs);  // idle ring + exchange area
-          if (leader) {
-            fence_proxy_async_all();
-            mbar_arrive_expect_tx(drain + 1, kH * 256 * 4);
-            for (int c = 0; c < 8; ++c)
-              bulk_load(po2 + c * 1024, p.part_o + other * (64 * kH) + c * 1024, 16384, drain + 1);
-          }
-          // merged in split order (split 0 first), whichever split runs the merge, so the
-          // result does not depend on which one finished last
-          const float mo = __ldcg(p.part_ml + (other * kH + h) * 2);
-          const float lo2 = __ldcg(p.part_ml + (other * kH + h) * 2 + 1);
-          const bool first = sp == 0;
-          const float m0 = first ? m_ref : mo, l0 = first ? ltot : lo2;
-          const float m1 = first ? mo : m_ref, l1 = first ? lo2 : ltot;
-          const float M = fmaxf(m0, m1);
-          const float w0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
-          const float w1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
-          const float wsum = w0 * l0 + w1 * l1;
-          const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-          if (!__all_sync(0xffffffffu, mbar_wait(drain + 1, 0, abort_flag, p.status,
-                                                 DSA_FLAG_TIMEOUT))) break;
-          uint8_t* orow = static_cast<uint8_t*>(p.out) +
-                          (((int64_t)t * kH + h) * kDC + gbase + ocol) * (p.out_f32 ? 4 : 2);
-          for (int b = 0; b < 4; ++b) {
-            uint32_t r[32];
-            if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
-            else
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 0u;
-            float o[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 x = po2[(32 * half + 8 * b + i) * kH + h];
-              const float xo[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float own = __uint_as_float(r[4 * i + e]);
-                const float a0 = first ? own : xo[e], a1 = first ? xo[e] : own;
-                o[4 * i + e] = (w0 * a0 + w1 * a1) * inv;
-              }
-            }
-            if (p.out_f32) {
-              float4* op = reinterpret_cast<float4*>(orow) + 8 * b;
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                op[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-            } else {
-              uint4* op = reinterpret_cast<uint4*>(orow) + 4 * b;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * i + 2 * e], o[8 * i + 2 * e + 1]);
-                  w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
-                }
-                op[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-              }
-            }
-          }
-          if (rank == 0 && half == 0 && p.lse)
-            p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f
-                                                    : -INFINITY;
-        }
       }
     }
   }
@@ -782,6 +735,74 @@ sfa_tc_kernel(Params p) {
   }
 }
 
+// Merge of the cut rows' pieces.  Thread = (query row t, CTA half `rank`, head h, group
+// of 8 column quads R = 8g .. 8g + 7, i.e. output columns gbase + 32g .. + 31); lanes run
+// along h, so every partial read is a coalesced 512-byte line, and a thread has 8 (or
+// 16) reads in flight.  With piece j's (O_j, m_j, l_j), M = max m_j over the pieces with
+// keys and w_j = 2^(m_j - M):  out = Σ_j w_j O_j / Σ_j w_j l_j, summed in piece order
+// (the same arithmetic whichever order the pieces finished in).
+__global__ void __launch_bounds__(256) sfa_combine_kernel(Params p) {
+  griddep_wait();  // the pieces' partials are complete
+  const int t = blockIdx.x >> 3;
+  const int rank = (blockIdx.x >> 2) & 1;
+  const int g = ((blockIdx.x & 3) << 1) | (threadIdx.x >> 7);
+  const int h = threadIdx.x & 127;
+  int cf, np;
+  row_pieces(p, t, p.nclusters, cf, np);
+  if (np == 1) return;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float M = -INFINITY;
+#pragma unroll 4
+  for (int j = 0; j < np; ++j) {
+    const float2 v = __ldg(ml + ((int64_t)(cf + j + t) * 2 + rank) * kH + h);
+    if (v.y > 0.f) M = fmaxf(M, v.x);
+  }
+  float wsum = 0.f;
+  float4 acc[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int j = 0; j < np; ++j) {
+    const int64_t sl = (int64_t)(cf + j + t) * 2 + rank;
+    const float2 v = __ldg(ml + sl * kH + h);
+    const float4* src = p.part_o + sl * (64 * kH) + (8 * g) * kH + h;
+    float4 x[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) x[r] = __ldg(src + r * kH);
+    const float w = v.y > 0.f ? ex2(v.x - M) : 0.f;
+    wsum = fmaf(w, v.y, wsum);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      acc[r].x = fmaf(w, x[r].x, acc[r].x);
+      acc[r].y = fmaf(w, x[r].y, acc[r].y);
+      acc[r].z = fmaf(w, x[r].z, acc[r].z);
+      acc[r].w = fmaf(w, x[r].w, acc[r].w);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int64_t o = ((int64_t)t * kH + h) * kDC + (rank ? 256 : 0) + 32 * g;
+  if (p.out_f32) {
+    float4* op = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      op[r] = make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
+  } else {
+    uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 a = acc[2 * i], b = acc[2 * i + 1];
+      const __nv_bfloat162 w0 = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+      const __nv_bfloat162 w1 = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+      const __nv_bfloat162 w2 = __floats2bfloat162_rn(b.x * inv, b.y * inv);
+      const __nv_bfloat162 w3 = __floats2bfloat162_rn(b.z * inv, b.w * inv);
+      op[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&w0), *reinterpret_cast<const uint32_t*>(&w1),
+                         *reinterpret_cast<const uint32_t*>(&w2), *reinterpret_cast<const uint32_t*>(&w3));
+    }
+  }
+  if (rank == 0 && g == 0 && p.lse)
+    p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+}
+
 }  // namespace
 
 bool sfa_tc_eligible(const SfaArgs& a) {
@@ -790,41 +811,30 @@ bool sfa_tc_eligible(const SfaArgs& a) {
          (reinterpret_cast<uintptr_t>(a.kv) & 15) == 0;
 }
 
-// Split each row over 2 clusters when that still leaves every cluster one unit.  With a
-// split, units = 2 * total_q <= num_sms / 2 = clusters, so a cluster never runs a second
-// unit: the merge may stage the partner's partial in the idle ring and exchange buffers.
-int sfa_tc_nsplit(int total_q) { return total_q > 0 && num_sms() >= 4 * total_q ? 2 : 1; }
+// Equal contiguous shares of the rows' chunk slots (pieces) when whole rows would load
+// the clusters unevenly: fewer than four rows per cluster.
+bool sfa_tc_pieces(int total_q) { return total_q > 0 && total_q < 2 * num_sms(); }
 
-// Per-CTA compacted key-row lists (the grid has at most num_sms CTAs), then, with a
-// split, the partial (O, m, l) slots and the per-row arrival counters.
+// Per-CTA compacted key-row lists (the grid has at most num_sms CTAs), then, with pieces,
+// the partial (O, m, l) slots: one per cluster and row it touches, slot = cluster + row <
+// total_q + clusters.
 size_t sfa_tc_scratch_bytes(int total_q) {
   const size_t lists = align_up((size_t)num_sms() * kMaxTopK * 4, 256);
-  const int ns = sfa_tc_nsplit(total_q);
-  if (ns == 1) return lists;
-  const size_t slots = (size_t)total_q * ns * 2;
-  return lists + align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256) +
-         align_up((size_t)total_q * 2 * 4, 256);
+  if (!sfa_tc_pieces(total_q)) return lists;
+  const size_t slots = ((size_t)total_q + num_sms() / 2) * 2;
+  return lists + align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256);
 }
 
-int sfa_tc_clear_counters(const SfaArgs& a, void* scratch, cudaStream_t stream) {
-  const int ns = sfa_tc_nsplit(a.seqs.total_q);
-  if (ns == 1 || a.seqs.total_q == 0) return DSA_OK;
-  const size_t slots = (size_t)a.seqs.total_q * ns * 2;
-  char* b = static_cast<char*>(scratch) + align_up((size_t)num_sms() * kMaxTopK * 4, 256) +
-            align_up(slots * kH * 256 * 4, 256) + align_up(slots * kH * 2 * 4, 256);
-  cudaError_t e = cudaMemsetAsync(b, 0, (size_t)a.seqs.total_q * 2 * 4, stream);
-  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
-  return DSA_OK;
-}
-
-int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream, bool counters_zeroed) {
+int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
-  const int ns = sfa_tc_nsplit(a.seqs.total_q);
+  const bool pieces = sfa_tc_pieces(a.seqs.total_q);
   Params p{};
   p.seqs = a.seqs;
   p.top_k = a.top_k;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.nsplit = ns;
+  p.pieces = pieces ? 1 : 0;
+  p.C = a.top_k > kNC ? (a.top_k + kNC - 1) / kNC : 1;
+  p.tot = (int64_t)a.seqs.total_q * p.C;
   p.out_f32 = a.out_dtype == DSA_F32;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.idx = a.idx;
@@ -835,29 +845,33 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream, bool cou
   char* b = static_cast<char*>(scratch);
   p.lists = reinterpret_cast<int32_t*>(b);
   b += align_up((size_t)num_sms() * kMaxTopK * 4, 256);
-  if (ns > 1) {
-    const size_t slots = (size_t)a.seqs.total_q * ns * 2;
+  if (pieces) {
+    const size_t slots = ((size_t)a.seqs.total_q + num_sms() / 2) * 2;
     p.part_o = reinterpret_cast<float4*>(b);
     b += align_up(slots * kH * 256 * 4, 256);
     p.part_ml = reinterpret_cast<float*>(b);
-    b += align_up(slots * kH * 2 * 4, 256);
-    p.counters = reinterpret_cast<int*>(b);
-    if (!counters_zeroed) {
-      const int rc = sfa_tc_clear_counters(a, scratch, stream);
-      if (rc != DSA_OK) return rc;
-    }
   }
   if (cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return check_launch("sfa_tc: smem attribute");
-  const int64_t units = (int64_t)a.seqs.total_q * ns;
+  const int64_t units = pieces ? p.tot : (int64_t)a.seqs.total_q;
   const int max_clusters = num_sms() / 2;
-  const int clusters = (int)(units < max_clusters ? units : max_clusters);
+  int clusters = (int)(units < max_clusters ? units : max_clusters);
+  // two clusters a row when that fits: shares end on half rows (two pieces a row), which
+  // beats a few more clusters whose shares cut rows into three or four pieces
+  if (pieces && 2 * a.seqs.total_q <= max_clusters && p.C % 2 == 0) clusters = 2 * a.seqs.total_q;
+  p.nclusters = clusters;
   cudaError_t e = cudaSuccess;
   DSA_LAUNCH("sfa_tc", stream,
              e = launch_pdl(sfa_tc_kernel, dim3(2 * clusters), dim3(kThreads), kSmem, stream, p));
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
-  return check_launch("sfa_tc");
+  int rc = check_launch("sfa_tc");
+  if (rc != DSA_OK || !pieces) return rc;
+  DSA_LAUNCH("sfa_combine", stream,
+             e = launch_pdl(sfa_combine_kernel, dim3((unsigned)a.seqs.total_q * 8), dim3(256), 0,
+                            stream, p));
+  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_combine: %s", cudaGetErrorString(e));
+  return check_launch("sfa_combine");
 }
 
 }  // namespace dsa

@@ -184,11 +184,13 @@ def test_sfa_flags_bad_indices_and_skips_them():
     assert ws.status() == 0
 
 
-@pytest.mark.parametrize("nq,out_dtype", [(3, "bf16"), (90, "bf16"), (5, "f32")])
+@pytest.mark.parametrize("nq,out_dtype", [(3, "bf16"), (90, "bf16"), (5, "f32"), (310, "bf16")])
 def test_tensor_core_sfa_standalone(nq, out_dtype):
-    # H = 128, d_c = 512, d_rope = 64 runs on tcgen05 CTA pairs; few queries split each row
-    # over several clusters (merged by the last one), many queries do not.  Index rows mix
-    # valid positions, -1 padding anywhere, out-of-range entries and a repeated entry.
+    # H = 128, d_c = 512, d_rope = 64 runs on tcgen05 CTA pairs.  Few queries (fewer than
+    # four per cluster) cut rows into pieces on equal shares of chunk slots, merged by the
+    # row's last piece (3 rows: up to ~25 pieces a row, many of them empty); 310 rows run
+    # whole rows.  Index rows mix valid positions, -1 padding anywhere, out-of-range
+    # entries and a repeated entry.
     L = 3000
     cfg = W.custom([nq], [L], h_idx=4, d_idx=32, h=128, d_c=512, d_rope=64, top_k=2048,
                    idx_dtype="bf16", kv_dtype="bf16", out_dtype=out_dtype)
