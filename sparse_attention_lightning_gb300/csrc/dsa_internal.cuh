@@ -88,10 +88,12 @@ void trace_pre(const char* name, cudaStream_t s);
 void trace_post(cudaStream_t s);
 int check_launch(const char* what);
 
-// A 2-D tiled tensor map (128-byte swizzle, 256-byte L2 promotion, zero fill):
-// `rows` rows of `inner` elements, `row_bytes` apart; box = box_inner x box_rows.
+// A 2-D tiled tensor map (128-byte swizzle unless `swizzle` is false, 256-byte L2
+// promotion, zero fill): `rows` rows of `inner` elements, `row_bytes` apart; box =
+// box_inner x box_rows.
 int make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                 uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+                 uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                 bool swizzle = true);
 int num_sms();
 
 #define DSA_LAUNCH(name, stream, ...)   \

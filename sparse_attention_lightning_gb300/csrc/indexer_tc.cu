@@ -67,8 +67,17 @@ struct Cfg {
   // per-row histograms: 32-bit counters for one row, 16-bit ones (flushed before they
   // can overflow) for a block of four
   static constexpr int HIST_BYTES = QB == 1 ? kHistBins * 4 : QB * kHistBins * 2;
-  static constexpr int MISC = 256 /*barriers*/ + EPI_WARPS * RPW * HI * 4 /*weights*/ + 64;
-  static constexpr int SMEM_FIXED = NS * KTILE + NQ * QTILE + HIST_BYTES + MISC + 1024 /*align*/;
+  // FP8: a ring of per-key scales, one slot per key tile: 132 floats from the tile's first
+  // key rounded down to a multiple of 4 (a TMA box must start 16-byte aligned), four
+  // more slots than key stages (the epilogue reads a tile's scales up to two tiles after
+  // its MMA has released the key stage)
+  static constexpr int NSC = FP8 ? NS + 4 : 0;
+  static constexpr int SC_BOX = BM + 4;
+  static constexpr int SC_BYTES = SC_BOX * 4;      // 528 bytes a box
+  static constexpr int SC_SLOT = 640;              // slot stride (128-byte aligned copies)
+  static constexpr int MISC = 512 /*barriers*/ + EPI_WARPS * RPW * HI * 4 /*weights*/ + 64;
+  static constexpr int SMEM_FIXED =
+      NS * KTILE + NQ * QTILE + HIST_BYTES + NSC * SC_SLOT + MISC + 1024 /*align*/;
   static_assert(TMEM_COLS <= 512, "TMEM");
 };
 
@@ -195,15 +204,18 @@ __device__ __forceinline__ uint32_t scan_block(uint32_t v, uint32_t* ws, uint32_
 template <bool FP8, int QB>
 __global__ void __launch_bounds__(Cfg<FP8, QB>::THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                  Params p) {
+                  const __grid_constant__ CUtensorMap smap, Params p) {
   using C = Cfg<FP8, QB>;
+  static_assert(2 * C::NS + 4 + 4 + 3 + C::NSC <= 64, "barrier area");
+  constexpr int NSCM = C::NSC > 0 ? C::NSC : 1;  // scale slots (as a modulus)
   constexpr int EPI_THREADS = 32 * C::EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* ks = smem;                                  // NS key tiles
   uint8_t* qs = ks + C::NS * C::KTILE;                 // NQ query blocks
   uint32_t* hs = reinterpret_cast<uint32_t*>(qs + C::NQ * C::QTILE);  // row-segment histograms
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(hs) + C::HIST_BYTES);
+  float* scs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(hs) + C::HIST_BYTES);  // NSC slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scs) + C::NSC * C::SC_SLOT);
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* q_full = k_empty + C::NS;
@@ -213,7 +225,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   uint64_t* drain = acc_empty + 2;
   uint64_t* epi_a = drain + 1;     // the epilogue threads: row segment scored
   uint64_t* epi_b = drain + 2;     // the epilogue threads: histograms flushed
-  float* wsm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [warps][RPW][64]
+  uint64_t* sc_empty = drain + 3;  // [NSC] FP8: the tile's epilogue warps have read its scales
+  float* wsm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);  // [warps][RPW][64]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsm + C::EPI_WARPS * C::RPW * C::HI);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* scan_ws = tmem_slot + 2;                   // [THREADS / 32]
@@ -269,10 +282,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     mbar_init(drain, 1);
     mbar_init(epi_a, EPI_THREADS);
     mbar_init(epi_b, EPI_THREADS);
+    for (int i = 0; i < C::NSC; ++i) mbar_init(&sc_empty[i], C::GROUP_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&kmap);
     prefetch_tmap(&qmap);
+    if (FP8) prefetch_tmap(&smap);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
   tc_fence_before();
@@ -303,10 +318,20 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int s = it % C::NS;
         if (!mbar_wait(&k_empty[s], ((it / C::NS) & 1) ^ 1, abort_flag, p.status,
                        DSA_FLAG_TIMEOUT)) break;
-        mbar_arrive_expect_tx(&k_full[s], C::KTILE);
+        const int key0 = cur.k0 + cur.j * C::BM;
+        if (FP8) {
+          // the tile's key scales land with its keys (the MMA waits for both)
+          const int sl = it % NSCM;
+          if (!mbar_wait(&sc_empty[sl], ((it / NSCM) & 1) ^ 1, abort_flag, p.status,
+                         DSA_FLAG_TIMEOUT)) break;
+          mbar_arrive_expect_tx(&k_full[s], C::KTILE + C::SC_BYTES);
+          tma_load_2d(scs + sl * (C::SC_SLOT / 4), &smap, &k_full[s], key0 & ~3, 0);
+        } else {
+          mbar_arrive_expect_tx(&k_full[s], C::KTILE);
+        }
         for (int a = 0; a < C::ATOMS; ++a)
           tma_load_2d_hint(ks + s * C::KTILE + a * (C::BM * 128), &kmap, &k_full[s],
-                           a * (128 / C::ES), cur.k0 + cur.j * C::BM, pol);
+                           a * (128 / C::ES), key0, pol);
         issued = it + 1;
       }
       // every copy issued has landed before the CTA may exit
@@ -365,11 +390,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     int nseg = 0, since = 0;
     Cursor<QB> cur;
     cur.locate(tabs, g0);
-    // FP8: the key scale of this thread's key (clamped to a real key of the block)
-    auto key_scale = [&](const Cursor<QB>& c) -> float {
-      const int s = min(c.j * C::BM + quarter * 32 + lane, c.pos + c.nrow - 1);
-      return __ldg(p.k_scale + c.k0 + s);
-    };
     float wreg[QB == 1 ? C::HI : 1];  // QB = 1: the row's head weights, in registers
     for (int g = g0, it = 0; g < g1; ++g, ++it) {
       if (g > g0) cur.advance(tabs);
@@ -395,13 +415,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       }
       const bool mine = C::GROUPS == 1 || (it & 1) == grp;
       if (mine) {
-      // issued before the wait for the accumulator, which hides its latency
-      const float ksc = FP8 ? key_scale(cur) : 1.f;
       const int acc = it & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it >> 1) & 1, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT)))
         break;
       tc_fence_after();
+      float ksc = 1.f;
+      if (FP8) {
+        // this thread's key scale, landed with the tile (its MMA waited for both); keys past
+        // the block read a neighbour's scale or the zero fill, and are not stored
+        const int sl = it % NSCM;
+        const int key0 = cur.k0 + cur.j * C::BM;
+        ksc = scs[sl * (C::SC_SLOT / 4) + (key0 & 3) + quarter * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc_empty[sl]);
+      }
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS +
                              rgrp * C::RPW * C::HI;
       // Σ_j w_j · ReLU(z_j) as four interleaved partial sums (a short dependency chain)
@@ -486,7 +514,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 template <bool FP8, int QB>
 int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
   using C = Cfg<FP8, QB>;
-  CUtensorMap kmap, qmap;
+  CUtensorMap kmap, qmap, smap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   int rc = make_tmap_2d(&kmap, dt, a.k_idx, C::DI, (uint64_t)a.seqs.total_k, C::ROWB,
                         128 / C::ES, C::BM);
@@ -494,6 +522,14 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
   rc = make_tmap_2d(&qmap, dt, a.q_idx, C::DI, (uint64_t)a.seqs.total_q * C::HI, C::ROWB,
                     128 / C::ES, C::N);
   if (rc != DSA_OK) return rc;
+  if (FP8) {
+    // k_scale as one row of total_k floats (no swizzle), read in boxes of 132
+    rc = make_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, (uint64_t)a.seqs.total_k,
+                      1, align_up((size_t)a.seqs.total_k * 4, 16), C::SC_BOX, 1, false);
+    if (rc != DSA_OK) return rc;
+  } else {
+    smap = kmap;  // unused
+  }
   const int smem = C::SMEM_FIXED + (int)align_up(3 * sizeof(int32_t) * (a.seqs.B + 1), 16);
   auto kern = indexer_tc_kernel<FP8, QB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -503,7 +539,7 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
   Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status, a.hist};
   DSA_LAUNCH(FP8 ? (QB == 1 ? "indexer_tc_fp8" : "indexer_tc_fp8_qb4")
                  : (QB == 1 ? "indexer_tc_bf16" : "indexer_tc_bf16_qb4"),
-             stream, kern<<<grid, C::THREADS, smem, stream>>>(kmap, qmap, p));
+             stream, kern<<<grid, C::THREADS, smem, stream>>>(kmap, qmap, smap, p));
   return check_launch("indexer_tc");
 }
 
@@ -512,8 +548,10 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
 bool indexer_tc_eligible(const IndexerArgs& a) {
   // tiles of the whole problem must stay below 2^31 (int32 item indices)
   const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + 127) / 128);
+  // (FP8: the key scales are read by TMA, which wants a 16-byte aligned base)
   return (a.idx_dtype == DSA_BF16 || a.idx_dtype == DSA_FP8_E4M3) && a.h_idx == 64 &&
-         a.d_idx == 128 && a.seqs.B <= kMaxSeqs && bound < (int64_t(1) << 31);
+         a.d_idx == 128 && a.seqs.B <= kMaxSeqs && bound < (int64_t(1) << 31) &&
+         (a.idx_dtype != DSA_FP8_E4M3 || (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0);
 }
 
 int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
