@@ -38,8 +38,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # any of them (their hash differs) makes the figure unknown again.
 MEASURED_TRAFFIC = {
     # (kernel, workload): (bytes per launch, sources, sha256 prefix of the sources)
-    ("sfa_tc", "decode"): (84_738_560, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                           "8d62f8db17fb287e"),
+    ("sfa_tc", "decode"): (83_125_248, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                           "48011cd94aab66f3"),
 }
 
 
@@ -230,6 +230,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8, help="oracle rows per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling: keep only the workload's first N sequences (same shapes)")
     args = ap.parse_args()
     if args.impl == "reference":
         os.environ.setdefault("OPENBLAS_NUM_THREADS", str(cores()))
@@ -246,6 +248,11 @@ def main():
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
 
     cfg = W.workload(args.workload)
+    if args.batch:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_first{args.batch}",
+                                  q_lens=list(cfg.q_lens[:args.batch]),
+                                  k_lens=list(cfg.k_lens[:args.batch]))
     seed = W.WORKLOAD_SEEDS[args.workload] + 1000 * rank
     if args.impl == "reference":
         if rank == 0:
@@ -331,14 +338,14 @@ def main():
         achieved = alg / (dom_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
-                "traffic": measured_traffic(dom, args.workload), "kernel": dom,
+                "traffic": measured_traffic(dom, args.workload if not args.batch else None), "kernel": dom,
                 "algorithmic_bytes_per_launch": alg, "peak_source": f"{peak_src} hbm_gbs"}
     else:
         alg = model[stage]["flops"]
         achieved = alg / (dom_ms / 1e3) / 1e12
         pk = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": measured_traffic(dom, args.workload),
+                "frac": achieved / pk, "traffic": measured_traffic(dom, args.workload if not args.batch else None),
                 "kernel": dom,
                 "algorithmic_flops_per_launch": alg, "peak_source": f"{peak_src} bf16_tflops"}
     roof["kernel_ms_mean"] = dom_ms
