@@ -224,6 +224,41 @@ def test_tensor_core_sfa_standalone(nq, out_dtype):
         check_attn_row(to_np(out)[t], to_np(lse)[t], ref_out, ref_lse, tol_for(cfg), f"row {t}")
 
 
+@pytest.mark.parametrize("nq,top_k", [(3, 1984), (41, 1984)])
+def test_tensor_core_sfa_rows_in_many_pieces(nq, top_k):
+    # top_k = 1984 gives 31 chunk slots a row (odd): the rows' slots are cut into 76 equal
+    # shares, so 3 rows spread over ~25 clusters each (pieces of 1-2 chunks, most of them
+    # holding only -1 padding) and 41 rows into pieces of ~16 chunks; the merge kernel
+    # combines every piece of a row.  Valid entries sit anywhere in the row.
+    L = 2600
+    cfg = W.custom([nq], [L], h_idx=4, d_idx=32, h=128, d_c=512, d_rope=64, top_k=top_k,
+                   idx_dtype="bf16", kv_dtype="bf16", out_dtype="bf16")
+    case = W.make_case(cfg, seed=43)
+    d = to_dev(case)
+    P = problem(case, d)
+    g = torch.Generator().manual_seed(100 + nq)
+    idx = torch.full((nq, top_k), -1, dtype=torch.int32)
+    for t in range(nq):
+        pos = L - nq + t
+        n = [top_k, 1, 200, 1500][t % 4]
+        sel = torch.randperm(pos + 1, generator=g)[:n].to(torch.int32)
+        slots = torch.randperm(top_k, generator=g)[:sel.numel()]
+        idx[t, slots] = sel
+    ws = dsa.Workspace()
+    ws.clear_status()
+    out, lse = dsa.sparse_mla_attn(P, d["q"], d["kv"], idx.cuda(), ws=ws)
+    assert ws.status() == 0
+    out2, lse2 = dsa.sparse_mla_attn(P, d["q"], d["kv"], idx.cuda(), ws=ws)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)), "merge not deterministic"
+    p = O.problem_from_case(case)
+    idn = idx.numpy()
+    for t in range(nq):
+        row = idn[t]
+        valid = row[row >= 0]
+        ref_out, ref_lse = p.sfa(t, valid)
+        check_attn_row(to_np(out)[t], to_np(lse)[t], ref_out, ref_lse, tol_for(cfg), f"row {t}")
+
+
 def test_repeat_runs_are_bitwise_identical():
     cfg = W.custom([1, 1], [3000, 2500], h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64,
                    top_k=2048, idx_dtype="bf16", kv_dtype="bf16")
