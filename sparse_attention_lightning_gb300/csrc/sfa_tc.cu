@@ -120,6 +120,24 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+// 64 consecutive TMEM columns of this warp's 32 lanes (one load, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Two floats to an f16 pair, rounded to nearest and saturated to the largest finite
+// magnitude (lo in the low half).
+__device__ __forceinline__ uint32_t f16x2_satfinite(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -471,22 +489,17 @@ sfa_tc_kernel(Params p) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], xph, abort_flag, p.status,
                                              DSA_FLAG_TIMEOUT))) return false;
       tc_fence_after();
+      {
+        uint32_t r[64];
+        tmem_ld64(lane_base + kSCol, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty);  // S is free for the next chunk's logit MMA
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + kSCol + 32 * hb, r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a = __uint_as_float(r[2 * e]) * p.scale_log2;
-          const float b = __uint_as_float(r[2 * e + 1]) * p.scale_log2;
-          const __half2 h2 = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f),
-                                               fminf(fmaxf(b, -65504.f), 65504.f));
-          own[16 * hb + e] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
+        for (int e = 0; e < 32; ++e)
+          own[e] = f16x2_satfinite(__uint_as_float(r[2 * e]) * p.scale_log2,
+                                   __uint_as_float(r[2 * e + 1]) * p.scale_log2);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
       // our x_full will take this chunk's bytes from the peer
       if (gleader) mbar_arrive_expect_tx(&x_full[grp], kXBytes);
       // the peer has read what we sent two chunks ago, so our copy of it is complete
