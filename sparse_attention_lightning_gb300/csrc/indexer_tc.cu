@@ -33,11 +33,13 @@
 // taking two of the block's rows).  Every wait is bounded (DSA_FLAG_TIMEOUT).
 #include "dsa_internal.cuh"
 #include "tc_sm100.cuh"
+#include "tile_sched.cuh"
 
 namespace dsa {
 namespace {
 
 using namespace tc;
+using namespace sched;
 
 constexpr int kMaxSeqs = 4096;  // sequences per launch on this path (tile table in smem)
 
@@ -93,90 +95,6 @@ struct Params {
   int64_t ld;
   uint32_t* status;
   uint32_t* hist;  // [total_q][kHistBins] or null
-};
-
-__device__ __forceinline__ int64_t ftiles(int64_t n) {  // Σ_{p<n} (floor(p/128) + 1)
-  const int64_t q = n >> 7, r = n & 127;
-  return n + 64 * q * (q - 1) + r * q;
-}
-
-// Σ_{x<n} floor(x / D)
-__device__ __forceinline__ int64_t gsum(int64_t n, int64_t D) {
-  const int64_t q = n / D, r = n % D;
-  return D * q * (q - 1) / 2 + r * q;
-}
-
-// Tiles of the first nb blocks of a sequence with T queries over L keys (nb <= full blocks).
-template <int QB>
-__device__ __forceinline__ int64_t block_tiles(int T, int L, int nb) {
-  if (QB == 1) return ftiles(L - T + nb) - ftiles(L - T);
-  const int64_t a = (L - T + QB - 1) / QB;
-  return nb + gsum(a + nb, 128 / QB) - gsum(a, 128 / QB);
-}
-
-// All tiles of a sequence.
-template <int QB>
-__device__ __forceinline__ int64_t seq_tiles(int T, int L) {
-  if (QB == 1) return ftiles(L) - ftiles(L - T);
-  const int nfull = T / QB;
-  return block_tiles<QB>(T, L, nfull) + (T % QB ? (L - 1) / 128 + 1 : 0);
-}
-
-// Per-sequence tile table built in shared memory by every CTA.
-struct SeqTab {
-  const int32_t* st;  // [B+1] first tile of each sequence, then the total
-  const int32_t* cq;  // [B+1] cu_q
-  const int32_t* ck;  // [B+1] cu_k
-  int B;
-};
-
-// Walks the CTA's items (block tile by block tile) in order; all roles run one.
-template <int QB>
-struct Cursor {
-  int b, ib, T, L, q0, k0;   // sequence, block index in it, its sizes and offsets
-  int t, pos, nrow, j, ntiles;  // first packed row of the block, its position, rows, tile
-
-  __device__ __forceinline__ void load_seq(const SeqTab& s) {
-    q0 = s.cq[b]; T = s.cq[b + 1] - q0;
-    k0 = s.ck[b]; L = s.ck[b + 1] - k0;
-  }
-  __device__ __forceinline__ void set_block() {
-    const int i0 = QB * ib;
-    t = q0 + i0;
-    pos = L - T + i0;
-    nrow = min(QB, T - i0);
-    ntiles = (pos + nrow - 1) / 128 + 1;
-  }
-  __device__ __forceinline__ void locate(const SeqTab& s, int g) {
-    int lo = 0, hi = s.B - 1;  // last b with st[b] <= g
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s.st[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-    load_seq(s);
-    const int64_t gl = g - s.st[b];
-    const int nfull = T / QB, nblk = (T + QB - 1) / QB;
-    int ilo = 0, ihi = nblk - 1;  // last block whose first tile is <= gl
-    while (ilo < ihi) {
-      const int mid = (ilo + ihi + 1) >> 1;
-      const int64_t before = mid <= nfull ? block_tiles<QB>(T, L, mid) : INT64_MAX;
-      if (before <= gl) ilo = mid; else ihi = mid - 1;
-    }
-    ib = ilo;
-    set_block();
-    j = (int)(gl - block_tiles<QB>(T, L, min(ib, nfull)));
-  }
-  __device__ __forceinline__ void advance(const SeqTab& s) {
-    if (++j < ntiles) return;
-    j = 0;
-    if (++ib * QB >= T) {
-      ib = 0;
-      do { ++b; } while (b < s.B - 1 && s.st[b + 1] == s.st[b]);  // skip tile-less sequences
-      load_seq(s);
-    }
-    set_block();
-  }
 };
 
 // Block-wide exclusive prefix sum over NW warps (two barriers).
