@@ -1,5 +1,5 @@
 // Blackwell (sm_100 family, built for sm_103a) building blocks in inline PTX:
-// mbarriers with bounded waits, TMA tensor loads (tiled and 4-row gather),
+// mbarriers with bounded waits, TMA tensor loads (tiled) and bulk copies,
 // tensor-memory allocation, tcgen05.mma with shared-memory descriptors,
 // tcgen05 commit/ld/st and the tcgen05 thread-sync fences.
 //
@@ -42,11 +42,6 @@ __device__ __forceinline__ void fence_barrier_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Order generic-proxy accesses (any state space) before later async-proxy ones.
-__device__ __forceinline__ void fence_proxy_async_all() {
-  asm volatile("fence.proxy.async;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -147,12 +142,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -170,18 +159,6 @@ __device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* sr
       "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           dst_cluster),
       "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
-// Four rows (r0..r3) of a 2-D tensor, columns [c0, c0 + box width), into four
-// consecutive smem rows at dst.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -315,17 +292,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 #undef DSA_W8
 
-// registers -> TMEM, 16 columns, followed by its wait.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
@@ -348,11 +314,6 @@ __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
                : "r"(taddr)
                : "memory");
   return v;
-}
-
-// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -388,71 +349,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_wait, with acquire at cluster scope (for arrivals from the peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort, uint32_t* status,
-                                                  uint32_t flag) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait_cluster(addr, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(addr, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        atomicOr(status, flag);
-        return false;
-      }
-    }
-  }
-}
-
-// Asynchronous remote store: 16 bytes into the peer CTA's shared memory, counted as
-// transaction bytes on the peer's mbarrier (no fence, the sender does not wait).
-__device__ __forceinline__ void st_async_f4(uint32_t cluster_addr, float4 v, uint32_t cluster_mbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          cluster_addr),
-      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_mbar)
-      : "memory");
-}
-
-__device__ __forceinline__ void st_async_u4(uint32_t cluster_addr, uint4 v, uint32_t cluster_mbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          cluster_addr),
-      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_mbar)
-      : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
-  return v;
 }
 
 }  // namespace tc

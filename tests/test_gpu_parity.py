@@ -284,8 +284,7 @@ def _sample_rows(T, k, n_random=24, seed=0):
     return sorted(fixed | set(rng.integers(0, T, n_random).tolist()))
 
 
-@pytest.mark.slow
-@pytest.mark.parametrize("name", ["prefill_8k", "prefill_64k"])
+@pytest.mark.parametrize("name", ["prefill_8k", pytest.param("prefill_64k", marks=pytest.mark.slow)])
 def test_prefill_workloads_sampled_rows(name):
     cfg = W.workload(name)
     case = W.make_case(cfg, W.WORKLOAD_SEEDS[name])
@@ -300,3 +299,15 @@ def test_fp8_decode_workload_sampled_sequences():
     P, out, lse, idx, vals = run_fused(case)
     rows = sorted(set(np.random.default_rng(4).integers(0, cfg.total_q, 14).tolist()) | {0, 127})
     check_rows(case, idx, vals, out, lse, rows)
+
+
+def test_fp8_decode_workload_first_sequences():
+    """The FP8-indexer decode workload's shapes (L = 131072, H_I = 64, d_I = 128, E4M3 with
+    per-token scales, bf16 latent), its first 16 sequences, every row checked."""
+    import dataclasses
+    cfg = W.workload("fp8_decode")
+    cfg = dataclasses.replace(cfg, name=cfg.name + "_first16", q_lens=list(cfg.q_lens[:16]),
+                              k_lens=list(cfg.k_lens[:16]))
+    case = W.make_case(cfg, W.WORKLOAD_SEEDS["fp8_decode"])
+    P, out, lse, idx, vals = run_fused(case)
+    check_rows(case, idx, vals, out, lse, range(cfg.total_q))
