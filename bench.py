@@ -104,7 +104,8 @@ def work_model(cfg):
 KERNEL_STAGE = {
     "indexer_scores_simt": "indexer", "indexer_tc_bf16": "indexer", "indexer_tc_fp8": "indexer",
     "indexer_tc_bf16_qb4": "indexer", "indexer_tc_fp8_qb4": "indexer",
-    "topk_rows": "topk", "topk_smem": "topk", "topk_cluster": "topk", "topk_stream": "topk",
+    "indexer_topk_bf16": "indexer", "indexer_topk_fp8": "indexer",
+    "topk_rows": "topk", "topk_smem": "topk", "topk_stream": "topk",
     "sfa_simt": "sfa", "sfa_tc": "sfa", "sfa_combine": "sfa_merge",
 }
 

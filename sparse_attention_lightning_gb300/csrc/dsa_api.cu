@@ -185,31 +185,57 @@ struct Carve {
 
 // Workspace score rows are padded to 32 floats (128 B) so every row is aligned.
 int64_t scores_ld(const dsa_problem* p) { return ((int64_t)p->max_k_len + 31) / 32 * 32; }
-size_t scores_bytes(const dsa_problem* p) { return (size_t)p->total_q * scores_ld(p) * 4; }
 size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 4; }
 
-// Fused indexer scratch: scores [total_q, max_k_len] f32, then the per-row tile
-// starts of the tensor-core schedule.  The fused forward adds the indices.
+IndexerArgs indexer_args(const dsa_problem* p, const void* q_idx, const void* k_idx,
+                         const float* w, const float* q_scale, const float* k_scale,
+                         void* ws) {
+  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3;
+  return IndexerArgs{seqs_of(p), p->h_idx, p->d_idx, p->idx_dtype, q_idx, k_idx, w,
+                     fp8 ? q_scale : nullptr, fp8 ? k_scale : nullptr,
+                     static_cast<uint32_t*>(ws)};
+}
+
+// Rows that carry their own history (decode) run the one-kernel fused indexer, which keeps
+// every score on chip and needs no scratch.  Prefill-shaped problems (several queries per
+// sequence: the tensor-core indexer scores blocks of four rows against each key tile) and
+// shapes that kernel does not cover score the rows in chunks: a chunk's scores go to a
+// bounded workspace buffer (sized for L2, not for the whole problem) and its Top-K reads
+// them back before the next chunk is scored.
+bool row_fused(const dsa_problem* p) {
+  const IndexerArgs ia = indexer_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  return indexer_topk_eligible(ia) && !indexer_tc_blocks4(ia);
+}
+bool tc_scores(const dsa_problem* p) {
+  const IndexerArgs ia = indexer_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  return indexer_tc_eligible(ia);
+}
+int64_t spill_ld(const dsa_problem* p) { return ((int64_t)p->max_k_len + 3) / 4 * 4; }
+
+// Bytes of chunk scratch per query row, and the rows of one chunk.
+constexpr size_t kChunkBudget = size_t(256) << 20;
+size_t chunk_row_bytes(const dsa_problem* p) {
+  size_t b = (size_t)scores_ld(p) * 4;
+  if (tc_scores(p)) b += (size_t)kHistBins * 4 + (size_t)spill_ld(p) * 4;
+  return b;
+}
+int chunk_rows(const dsa_problem* p) {
+  if (p->total_q == 0 || row_fused(p)) return 0;
+  size_t r = kChunkBudget / chunk_row_bytes(p);
+  if (r < 1) r = 1;
+  return (int)(r < (size_t)p->total_q ? r : (size_t)p->total_q);
+}
+
+// Fused indexer scratch (chunked path only): a chunk's scores [rows][scores_ld] f32,
+// histograms [rows][kHistBins] and Top-K candidate positions [rows][spill_ld]; then the
+// fused forward's indices and the attention scratch.
 struct IndexerScratch {
   float* scores;
-  uint32_t* hist;       // [total_q][kHistBins]: cleared per call
-  int32_t* spill;       // [total_q][spill_ld]: a row's Top-K candidates beyond shared memory
+  uint32_t* hist;
+  int32_t* spill;
   int32_t* idx;
   void* sfa;
 };
-
-// The tensor-core indexer also histograms each row, which seeds the Top-K kernels.
-bool use_topk_hist(const dsa_problem* p) {
-  return (p->idx_dtype == DSA_BF16 || p->idx_dtype == DSA_FP8_E4M3) && p->h_idx == 64 &&
-         p->d_idx == 128 && p->num_seqs <= 4096;
-}
-size_t hist_bytes(const dsa_problem* p) {
-  return use_topk_hist(p) ? (size_t)p->total_q * kHistBins * 4 : 0;
-}
-int64_t spill_ld(const dsa_problem* p) { return ((int64_t)p->max_k_len + 3) / 4 * 4; }
-size_t spill_bytes(const dsa_problem* p) {
-  return use_topk_hist(p) ? (size_t)p->total_q * spill_ld(p) * 4 : 0;
-}
 
 // SFA scratch of the tensor-core path (per-CTA key-row lists, split-row partials).
 size_t sfa_scratch_bytes(const dsa_problem* p) {
@@ -219,15 +245,17 @@ size_t sfa_scratch_bytes(const dsa_problem* p) {
 
 size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
-  const size_t o_scores = c.take(scores_bytes(p));
-  const size_t o_hist = c.take(hist_bytes(p));
-  const size_t o_spill = c.take(spill_bytes(p));
+  const size_t rows = (size_t)chunk_rows(p);
+  const bool tc = tc_scores(p);
+  const size_t o_scores = c.take(rows * scores_ld(p) * 4);
+  const size_t o_hist = c.take(tc ? rows * kHistBins * 4 : 0);
+  const size_t o_spill = c.take(tc ? rows * spill_ld(p) * 4 : 0);
   const size_t o_idx = c.take(idx_bytes(p));
   const size_t o_sfa = c.take(sfa_scratch_bytes(p));
   if (out) {
     char* b = static_cast<char*>(ws);
     out->scores = reinterpret_cast<float*>(b + o_scores);
-    out->hist = hist_bytes(p) ? reinterpret_cast<uint32_t*>(b + o_hist) : nullptr;
+    out->hist = tc ? reinterpret_cast<uint32_t*>(b + o_hist) : nullptr;
     out->spill = reinterpret_cast<int32_t*>(b + o_spill);
     out->idx = reinterpret_cast<int32_t*>(b + o_idx);
     out->sfa = b + o_sfa;
@@ -270,15 +298,6 @@ int check_indexer_inputs(const dsa_problem* p, const void* q_idx, const void* k_
   return DSA_OK;
 }
 
-IndexerArgs indexer_args(const dsa_problem* p, const void* q_idx, const void* k_idx,
-                         const float* w, const float* q_scale, const float* k_scale,
-                         void* ws) {
-  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3;
-  return IndexerArgs{seqs_of(p), p->h_idx, p->d_idx, p->idx_dtype, q_idx, k_idx, w,
-                     fp8 ? q_scale : nullptr, fp8 ? k_scale : nullptr,
-                     static_cast<uint32_t*>(ws)};
-}
-
 int run_topk(const TopkArgs& ta, cudaStream_t s) {
   if (ta.seqs.max_k_len <= topk_smem_max_keys()) return launch_topk_smem(ta, s);
   return launch_topk_rows(ta, s);
@@ -287,25 +306,33 @@ int run_topk(const TopkArgs& ta, cudaStream_t s) {
 int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx, const float* w,
                       const float* q_scale, const float* k_scale, int32_t* idx, float* vals,
                       void* ws, cudaStream_t s) {
+  IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
+  if (row_fused(p)) return launch_indexer_topk(ia, p->top_k, idx, vals, s);
   IndexerScratch sc;
   carve_indexer(p, ws, &sc);
-  IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
   const int64_t ld = scores_ld(p);
-  uint32_t* hist = nullptr;
-  if (indexer_tc_eligible(ia)) {
-    ia.hist = hist = sc.hist;
-    if (hist) {
-      cudaError_t e = cudaMemsetAsync(hist, 0, hist_bytes(p), s);
+  const bool tc = tc_scores(p);
+  const int rows = chunk_rows(p);
+  for (int r0 = 0; r0 < p->total_q; r0 += rows) {
+    const int r1 = r0 + rows < p->total_q ? r0 + rows : p->total_q;
+    ia.row0 = r0;
+    ia.row1 = r1;
+    TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws)};
+    ta.row0 = r0;
+    ta.nrows = r1 - r0;
+    if (tc) {
+      ia.hist = sc.hist;
+      cudaError_t e = cudaMemsetAsync(sc.hist, 0, (size_t)(r1 - r0) * kHistBins * 4, s);
       if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "hist clear: %s", cudaGetErrorString(e));
+      DSA_TRY(launch_indexer_tc(ia, sc.scores, ld, s));
+      ta.hist = sc.hist;
+      DSA_TRY(launch_topk_stream(ta, sc.spill, spill_ld(p), s));
+    } else {
+      DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, ld, s));
+      DSA_TRY(run_topk(ta, s));
     }
-    DSA_TRY(launch_indexer_tc(ia, sc.scores, ld, s));
-  } else {
-    DSA_TRY(launch_indexer_scores_simt(ia, sc.scores, ld, s));
   }
-  TopkArgs ta{seqs_of(p), p->top_k, sc.scores, ld, idx, vals, static_cast<uint32_t*>(ws), hist};
-  if (hist && topk_cluster_eligible(ta)) return launch_topk_cluster(ta, s);
-  if (hist) return launch_topk_stream(ta, sc.spill, spill_ld(p), s);
-  return run_topk(ta, s);
+  return DSA_OK;
 }
 
 SfaArgs sfa_args(const dsa_problem* p, const void* q, const void* kv, const int32_t* idx,

@@ -140,6 +140,9 @@ struct IndexerArgs {
   const float* k_scale;
   uint32_t* status;
   uint32_t* hist = nullptr;  // tensor-core path: also fill the Top-K histogram (zero on entry)
+  // Only the packed query rows [row0, row1) are scored; their scores (and histograms) go
+  // to rows t - row0 of the output.
+  int row0 = 0, row1 = 0x7fffffff;
 };
 
 int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
@@ -148,6 +151,15 @@ int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
 // tcgen05 indexer (H_I = 64, d_I = 128, bf16 or FP8): writes scores[t, s] for s <= pos(t).
 bool indexer_tc_eligible(const IndexerArgs& a);
 int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream);
+// Whether the tcgen05 indexer scores blocks of four query rows (prefill-shaped problems).
+bool indexer_tc_blocks4(const IndexerArgs& a);
+
+// The fused indexer for rows that carry their own history (decode): scores, head weights
+// and the causal Top-K in one kernel, one thread-block cluster per row, scores kept in
+// tensor memory; writes idx (ascending positions, -1 padded) and optionally vals.
+bool indexer_topk_eligible(const IndexerArgs& a);
+int launch_indexer_topk(const IndexerArgs& a, int top_k, int32_t* idx, float* vals,
+                        cudaStream_t stream);
 
 // Fill scores[t, s] = -inf for pos(t) < s < ld.
 int launch_mask_tail(const Seqs& seqs, float* scores, int64_t ld, uint32_t* status,
@@ -164,19 +176,20 @@ struct TopkArgs {
   int32_t* idx;
   float* vals;
   uint32_t* status;
-  const uint32_t* hist = nullptr;  // [total_q][kHistBins] or null
+  const uint32_t* hist = nullptr;  // [rows][kHistBins] or null
+  // Only the packed query rows [row0, row0 + nrows) are selected (nrows < 0: all); their
+  // scores (and histograms) are rows t - row0 of `scores` (and `hist`).
+  int row0 = 0, nrows = -1;
+  __host__ __device__ int rows() const { return nrows < 0 ? seqs.total_q - row0 : nrows; }
 };
 int launch_topk_rows(const TopkArgs& a, cudaStream_t stream);
 // Shared-memory-resident variant for rows of at most topk_smem_max_keys() keys.
 int topk_smem_max_keys();
 int launch_topk_smem(const TopkArgs& a, cudaStream_t stream);
-// One 256-thread CTA streaming each row, histogram-seeded (a.hist set): for many rows.
-// buf [total_q][buf_ld] int32, buf_ld >= max_k_len: candidates of rows that do not fit
+// One 256-thread CTA streaming each row, histogram-seeded (a.hist set).
+// buf [rows][buf_ld] int32, buf_ld >= max_k_len: candidates of rows that do not fit
 // in shared memory.
 int launch_topk_stream(const TopkArgs& a, int32_t* buf, int64_t buf_ld, cudaStream_t stream);
-// One thread-block cluster (up to 8 CTAs) per row, histogram-seeded (a.hist set).
-bool topk_cluster_eligible(const TopkArgs& a);
-int launch_topk_cluster(const TopkArgs& a, cudaStream_t stream);
 
 struct SfaArgs {
   Seqs seqs;

@@ -30,7 +30,7 @@ indexer_scores_simt_kernel(IndexerArgs a, float* __restrict__ scores, int64_t ld
   float* ks = wsm + HI;                     // [64][DI + 1]
   float* red = ks + kKeysPerCta * (DI + 1); // [4][64]
 
-  const int t = blockIdx.x;
+  const int t = a.row0 + blockIdx.x;
   const int tid = threadIdx.x;
   RowInfo r;
   if (!query_row_info(a.seqs, t, r, a.status)) return;
@@ -48,7 +48,7 @@ indexer_scores_simt_kernel(IndexerArgs a, float* __restrict__ scores, int64_t ld
 
   for (int64_t s0 = (int64_t)blockIdx.y * kKeysPerCta; s0 < ld;
        s0 += (int64_t)gridDim.y * kKeysPerCta) {
-    float* out = scores + (int64_t)t * ld + s0;
+    float* out = scores + (int64_t)blockIdx.x * ld + s0;
     if (s0 > r.pos) {  // whole tile in the future: masked
       for (int i = tid; i < kKeysPerCta && s0 + i < ld; i += kThreads) out[i] = -INFINITY;
       continue;
@@ -96,7 +96,9 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
       cudaSuccess)
     return check_launch("indexer_scores_simt: smem attribute");
   const int64_t tiles = (ld + kKeysPerCta - 1) / kKeysPerCta;
-  dim3 grid(a.seqs.total_q, (unsigned)(tiles < 65535 ? tiles : 65535));
+  const int rows = (a.row1 < a.seqs.total_q ? a.row1 : a.seqs.total_q) - a.row0;
+  if (rows <= 0) return DSA_OK;
+  dim3 grid((unsigned)rows, (unsigned)(tiles < 65535 ? tiles : 65535));
   DSA_LAUNCH("indexer_scores_simt", stream,
              kern<<<grid, kThreads, smem, stream>>>(a, scores, ld));
   return check_launch("indexer_scores_simt");

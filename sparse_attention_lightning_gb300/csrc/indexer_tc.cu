@@ -91,10 +91,11 @@ struct Params {
   const float* w;
   const float* q_scale;
   const float* k_scale;
-  float* scores;
+  float* scores;    // row t - r0 holds query row t
   int64_t ld;
   uint32_t* status;
-  uint32_t* hist;  // [total_q][kHistBins] or null
+  uint32_t* hist;  // [rows][kHistBins] or null (row t - r0)
+  int r0, r1;      // the packed query rows scored
 };
 
 // Block-wide exclusive prefix sum over NW warps (two barriers).
@@ -167,7 +168,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       const int T = q1 - q0, L = k1 - k0;
       const bool ok = q0 >= 0 && T >= 0 && T <= L && k0 >= 0 && k1 <= p.seqs.total_k &&
                       L <= p.seqs.max_k_len && q1 <= p.seqs.total_q;
-      if (ok) n = (uint32_t)seq_tiles<QB>(T, L);
+      int cq0, cT, cL;  // the sequence restricted to the rows scored
+      clip_seq(q0, q1, k0, k1, p.r0, p.r1, cq0, cT, cL);
+      if (ok) n = (uint32_t)seq_tiles<QB>(cT, cL);
       else if (blockIdx.x == 0) atomicOr(p.status, DSA_FLAG_BAD_SEQS);
       cq[b] = q0;
       ck[b] = k0;
@@ -185,7 +188,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     ck[B] = __ldg(p.seqs.cu_k + B);
   }
   __syncthreads();
-  const SeqTab tabs{st, cq, ck, B};
+  SeqTab tabs{st, cq, ck, B};
+  tabs.r0 = p.r0;
+  tabs.r1 = p.r1;
   const int total = st[B];
   const int g0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int g1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
@@ -377,7 +382,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const bool valid = r < cur.nrow && s <= cur.pos + r;
         float v = sum[rr];
         if (FP8) v *= ksc;
-        if (valid) p.scores[(int64_t)(cur.t + r) * p.ld + s] = v;
+        if (valid) p.scores[(int64_t)(cur.t + r - p.r0) * p.ld + s] = v;
         if (p.hist) {
           // scores of neighbouring keys share bins: one shared-memory atomic per bin per warp
           if (valid) {
@@ -396,7 +401,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (!__all_sync(0xffffffffu, mbar_wait(epi_a, nseg & 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT))) break;
         if (QB == 1) {
-          uint32_t* grow = p.hist + (int64_t)cur.t * kHistBins;
+          uint32_t* grow = p.hist + (int64_t)(cur.t - p.r0) * kHistBins;
           for (int bin = e; bin < kHistBins; bin += EPI_THREADS) {
             const uint32_t v = hs[bin];
             if (v) { atomicAdd(grow + bin, v); hs[bin] = 0u; }
@@ -406,7 +411,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const uint32_t v = hs[wi];
             if (v) {
               const int r = wi / (kHistBins / 2), b0 = 2 * (wi % (kHistBins / 2));
-              uint32_t* grow = p.hist + (int64_t)(cur.t + r) * kHistBins;
+              uint32_t* grow = p.hist + (int64_t)(cur.t + r - p.r0) * kHistBins;
               if (v & 0xffffu) atomicAdd(grow + b0, v & 0xffffu);
               if (v >> 16) atomicAdd(grow + b0 + 1, v >> 16);
               hs[wi] = 0u;
@@ -452,9 +457,11 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
   auto kern = indexer_tc_kernel<FP8, QB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("indexer_tc: smem attribute");
-  const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + C::BM - 1) / C::BM);
+  const int r1 = a.row1 < a.seqs.total_q ? a.row1 : a.seqs.total_q;
+  if (r1 <= a.row0) return DSA_OK;
+  const int64_t bound = (int64_t)(r1 - a.row0) * ((a.seqs.max_k_len + C::BM - 1) / C::BM);
   const int grid = (int)(bound < num_sms() ? bound : num_sms());
-  Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status, a.hist};
+  Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status, a.hist, a.row0, r1};
   DSA_LAUNCH(FP8 ? (QB == 1 ? "indexer_tc_fp8" : "indexer_tc_fp8_qb4")
                  : (QB == 1 ? "indexer_tc_bf16" : "indexer_tc_bf16_qb4"),
              stream, kern<<<grid, C::THREADS, smem, stream>>>(kmap, qmap, smap, p));
@@ -472,10 +479,14 @@ bool indexer_tc_eligible(const IndexerArgs& a) {
          (a.idx_dtype != DSA_FP8_E4M3 || (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0);
 }
 
+// blocks of four query rows when sequences hold several queries each (prefill)
+bool indexer_tc_blocks4(const IndexerArgs& a) {
+  return a.seqs.B <= kQBMaxSeqs && a.seqs.total_q >= 4 * a.seqs.B;
+}
+
 int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
-  // blocks of four query rows when sequences hold several queries each (prefill)
-  const bool qb4 = a.seqs.B <= kQBMaxSeqs && a.seqs.total_q >= 4 * a.seqs.B;
+  const bool qb4 = indexer_tc_blocks4(a);
   if (a.idx_dtype == DSA_FP8_E4M3)
     return qb4 ? launch_typed<true, 4>(a, scores, ld, stream)
                : launch_typed<true, 1>(a, scores, ld, stream);

@@ -54,12 +54,25 @@ DSA_HD_INLINE int64_t seq_tiles(int T, int L) {
   return block_tiles<QB>(T, L, nfull) + (T % QB ? (L - 1) / 128 + 1 : 0);
 }
 
+// A sequence's queries restricted to the packed rows [r0, r1): the rows it keeps are
+// [q0, q0 + T) and, being the last T of the first L keys' positions, they sit where they
+// sat in the whole sequence (the keys after the last kept row are simply not visible).
+// T = 0 when the sequence has no row in the range.
+DSA_HD_INLINE void clip_seq(int qa, int qe, int ka, int ke, int r0, int r1, int& q0, int& T,
+                            int& L) {
+  const int a = qa > r0 ? qa : r0, e = qe < r1 ? qe : r1;
+  q0 = a;
+  T = e > a ? e - a : 0;
+  L = T > 0 ? (ke - ka) - (qe - qa) + (e - qa) : 0;
+}
+
 // Per-sequence tile table built in shared memory by every CTA.
 struct SeqTab {
   const int32_t* st;  // [B+1] first tile of each sequence, then the total
   const int32_t* cq;  // [B+1] cu_q
   const int32_t* ck;  // [B+1] cu_k
   int B;
+  int r0 = 0, r1 = 0x7fffffff;  // the packed query rows scored (all by default)
 };
 
 // Walks the CTA's items (block tile by block tile) in order; all roles run one.
@@ -69,8 +82,8 @@ struct Cursor {
   int t, pos, nrow, j, ntiles;  // first packed row of the block, its position, rows, tile
 
   DSA_HD_INLINE void load_seq(const SeqTab& s) {
-    q0 = s.cq[b]; T = s.cq[b + 1] - q0;
-    k0 = s.ck[b]; L = s.ck[b + 1] - k0;
+    clip_seq(s.cq[b], s.cq[b + 1], s.ck[b], s.ck[b + 1], s.r0, s.r1, q0, T, L);
+    k0 = s.ck[b];
   }
   DSA_HD_INLINE void set_block() {
     const int i0 = QB * ib;

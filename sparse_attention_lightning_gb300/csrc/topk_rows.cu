@@ -50,10 +50,10 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(TopkArgs a) {
   __shared__ uint32_t warp_sums[kWarps];
   __shared__ uint32_t s_digit, s_above;
 
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int t = a.row0 + blockIdx.x, tid = threadIdx.x;  // scores: row blockIdx.x
   RowInfo r;
   if (!query_row_info(a.seqs, t, r, a.status)) return;
-  const float* row = a.scores + (int64_t)t * a.ld;
+  const float* row = a.scores + (int64_t)blockIdx.x * a.ld;
   const int n = r.pos + 1;
   const int k = min(a.top_k, n);
   int32_t* idx = a.idx + (int64_t)t * a.top_k;
@@ -139,9 +139,9 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(TopkArgs a) {
 }  // namespace
 
 int launch_topk_rows(const TopkArgs& a, cudaStream_t stream) {
-  if (a.seqs.total_q == 0) return DSA_OK;
+  if (a.rows() <= 0) return DSA_OK;
   DSA_LAUNCH("topk_rows", stream,
-             topk_rows_kernel<<<a.seqs.total_q, kThreads, 0, stream>>>(a));
+             topk_rows_kernel<<<a.rows(), kThreads, 0, stream>>>(a));
   return check_launch("topk_rows");
 }
 

@@ -41,10 +41,11 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   __shared__ uint32_t red_min[kW], red_max[kW];
   __shared__ uint32_t s_digit, s_above, s_cnt, s_ncand;
 
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = a.row0 + blockIdx.x;  // query row; its scores are row blockIdx.x
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   RowInfo r;
   if (!query_row_info(a.seqs, t, r, a.status)) return;
-  const float* row = a.scores + (int64_t)t * a.ld;
+  const float* row = a.scores + (int64_t)blockIdx.x * a.ld;
   const int n = r.pos + 1;
   const int k = min(a.top_k, n);
   int32_t* idx = a.idx + (int64_t)t * a.top_k;
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(kT, 1) topk_smem_kernel(TopkArgs a) {
   uint32_t hb_bin = 0, hb_above = 0, hb_cnt = 0;
   const bool use_hist = a.hist != nullptr;
   if (use_hist) {
-    const uint4* hrow = reinterpret_cast<const uint4*>(a.hist + (int64_t)t * kHistBins);
+    const uint4* hrow = reinterpret_cast<const uint4*>(a.hist + (int64_t)blockIdx.x * kHistBins);
     const uint4 c4 = __ldcg(hrow + tid);  // bins 4*tid .. 4*tid+3
     if (k < n) {
       // keys in bins above this thread's: exclusive scan in descending bin order
@@ -306,11 +307,11 @@ __global__ void mask_tail_kernel(Seqs seqs, float* scores, int64_t ld, uint32_t*
 int topk_smem_max_keys() { return kMaxKeys; }
 
 int launch_topk_smem(const TopkArgs& a, cudaStream_t stream) {
-  if (a.seqs.total_q == 0) return DSA_OK;
+  if (a.rows() <= 0) return DSA_OK;
   if (cudaFuncSetAttribute(topk_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmem) != cudaSuccess)
     return check_launch("topk_smem: smem attribute");
-  DSA_LAUNCH("topk_smem", stream, topk_smem_kernel<<<a.seqs.total_q, kT, kSmem, stream>>>(a));
+  DSA_LAUNCH("topk_smem", stream, topk_smem_kernel<<<a.rows(), kT, kSmem, stream>>>(a));
   return check_launch("topk_smem");
 }
 

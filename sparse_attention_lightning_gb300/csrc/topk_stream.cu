@@ -133,14 +133,15 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
                                                          int64_t spill_ld) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ShS& S = *reinterpret_cast<ShS*>(smem_raw);
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
+  const int t = a.row0 + blockIdx.x;  // query row; its scores are row blockIdx.x
   RowInfo r;
   if (!query_row_info(a.seqs, t, r, a.status)) return;
   const int n = r.pos + 1;
   const int k = min(a.top_k, n);
   griddep_wait();                  // the scores and histograms are complete
   if (tid == 0) griddep_launch();  // the attention kernel may be scheduled (it waits)
-  const float* row = a.scores + (int64_t)t * a.ld;
+  const float* row = a.scores + (int64_t)blockIdx.x * a.ld;
   int32_t* irow = a.idx + (int64_t)t * a.top_k;
   float* vrow = a.vals ? a.vals + (int64_t)t * a.top_k : nullptr;
 
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
 
   // ---- threshold bin: thread tid owns bins 16 tid .. 16 tid + 15 ----
   {
-    const uint4* h4 = reinterpret_cast<const uint4*>(a.hist + (int64_t)t * kHistBins) + 4 * tid;
+    const uint4* h4 = reinterpret_cast<const uint4*>(a.hist + (int64_t)blockIdx.x * kHistBins) + 4 * tid;
     uint32_t c[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
   }
   const uint32_t bstar = S.s_bin, above = S.s_above, nc = S.s_cnt;
   const bool in_smem = nc <= (uint32_t)kCap;
-  int32_t* gpos = spill + (int64_t)t * spill_ld;
+  int32_t* gpos = spill + (int64_t)blockIdx.x * spill_ld;
   auto cand = [&](uint32_t c) -> uint2 {  // (key, position) of candidate c
     if (in_smem) return S.cand[c];
     const int32_t p = gpos[c];
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
 }  // namespace
 
 int launch_topk_stream(const TopkArgs& a, int32_t* buf, int64_t buf_ld, cudaStream_t stream) {
-  if (a.seqs.total_q == 0) return DSA_OK;
+  if (a.rows() <= 0) return DSA_OK;
   const size_t smem = sizeof(ShS);
   if (cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
@@ -349,7 +350,7 @@ int launch_topk_stream(const TopkArgs& a, int32_t* buf, int64_t buf_ld, cudaStre
   // candidates of a row that does not fit in shared memory: their positions in the row's
   // slot of the workspace buffer (buf_ld >= max_k_len entries)
   DSA_LAUNCH("topk_stream", stream,
-             e = launch_pdl(topk_stream_kernel, dim3((unsigned)a.seqs.total_q), dim3(kT), smem,
+             e = launch_pdl(topk_stream_kernel, dim3((unsigned)a.rows()), dim3(kT), smem,
                             stream, a, buf, buf_ld));
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "topk_stream: %s", cudaGetErrorString(e));
   return check_launch("topk_stream");

@@ -14,15 +14,28 @@ struct Item {
   int b, ib, j;
 };
 
+// Whole sequences (T0, L0) restricted to the packed query rows [r0, r1): brute force on
+// the clipped sequences (T, L, first row q0) against the header's closed forms and cursor.
 template <int QB>
-static bool check(const std::vector<int>& T, const std::vector<int>& L) {
-  const int B = (int)T.size();
+static bool check(const std::vector<int>& T0, const std::vector<int>& L0, int r0 = 0,
+                  int r1 = 0x7fffffff) {
+  const int B = (int)T0.size();
   std::vector<int32_t> st(B + 1), cq(B + 1), ck(B + 1);
+  std::vector<int> T(B), L(B), q0(B);
   cq[0] = ck[0] = st[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    cq[b + 1] = cq[b] + T0[b];
+    ck[b + 1] = ck[b] + L0[b];
+    // brute-force clip: the rows of sequence b inside [r0, r1), their keys
+    int first = -1, cnt = 0;
+    for (int r = cq[b]; r < cq[b + 1]; ++r)
+      if (r >= r0 && r < r1) { if (first < 0) first = r; ++cnt; }
+    T[b] = cnt;
+    q0[b] = cnt ? first : 0;
+    L[b] = cnt ? L0[b] - T0[b] + (first - cq[b]) + cnt : 0;
+  }
   std::vector<Item> items;
   for (int b = 0; b < B; ++b) {
-    cq[b + 1] = cq[b] + T[b];
-    ck[b + 1] = ck[b] + L[b];
     int64_t n = 0, full = 0;
     const int nfull = T[b] / QB;
     for (int ib = 0; ib * QB < T[b]; ++ib) {
@@ -50,11 +63,13 @@ static bool check(const std::vector<int>& T, const std::vector<int>& L) {
     st[b + 1] = st[b] + (int32_t)n;
   }
   if ((size_t)st[B] != items.size()) return false;
-  const SeqTab tab{st.data(), cq.data(), ck.data(), B};
+  SeqTab tab{st.data(), cq.data(), ck.data(), B};
+  tab.r0 = r0;
+  tab.r1 = r1;
   auto same = [&](const Cursor<QB>& c, int g) {
     const Item& it = items[g];
     const int i0 = QB * it.ib;
-    return c.b == it.b && c.ib == it.ib && c.j == it.j && c.t == cq[it.b] + i0 &&
+    return c.b == it.b && c.ib == it.ib && c.j == it.j && c.t == q0[it.b] + i0 &&
            c.pos == L[it.b] - T[it.b] + i0;
   };
   const int total = st[B];
@@ -94,6 +109,15 @@ int main() {
       T[b] = kind == 0 ? 0 : kind == 1 ? L[b] : kind == 2 ? 1 : (int)(rng() % (L[b] + 1));
     }
     if (!check<1>(T, L) || !check<4>(T, L)) return 1;
+    // the same problem restricted to a random range of packed query rows
+    int tq = 0;
+    for (int b = 0; b < B; ++b) tq += T[b];
+    const int a = tq ? (int)(rng() % tq) : 0;
+    const int e = a + (tq ? (int)(rng() % (tq - a + 1)) : 0);
+    if (!check<1>(T, L, a, e) || !check<4>(T, L, a, e)) {
+      std::printf("  (rows %d..%d)\n", a, e);
+      return 1;
+    }
     ++cases;
   }
   // the first and last sequences tile-less, and exact 128 / 4 multiples
