@@ -233,6 +233,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="profiling: keep only the workload's first N sequences (same shapes)")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="read the key caches through a block table of pages of this many rows "
+                         "(pages in a seeded random order)")
     args = ap.parse_args()
     if args.impl == "reference":
         os.environ.setdefault("OPENBLAS_NUM_THREADS", str(cores()))
@@ -271,7 +274,13 @@ def main():
 
     case = W.make_case(cfg, seed)
     d = {k: v.to(dev) for k, v in case.tensors().items()}
-    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"])
+    paging = {}
+    if args.page_size:
+        pk = W.paged_keys(case, args.page_size, seed)
+        d.update({k: v.to(dev) for k, v in pk.tensors().items()})
+        paging = dict(block_table=d["block_table"], page_size=args.page_size,
+                      num_pages=pk.num_pages)
+    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"], **paging)
     ws = dsa.Workspace(dev, P.workspace_size(5))
     out = torch.empty(cfg.total_q, cfg.h, cfg.d_c, dtype=torch.bfloat16 if cfg.out_dtype == "bf16"
                       else torch.float32, device=dev)
@@ -447,7 +456,9 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.kv_dtype if cfg.idx_dtype != "e4m3" else "e4m3+bf16",
             "data": "synthetic (seeded N(0,1/sqrt(d)) values, w~U(0,1))",
-            "config": {"workload": describe(cfg), "tokens_per_step_per_gpu": cfg.total_q,
+            "config": {"workload": describe(cfg) + (f" paged={args.page_size}" if args.page_size
+                                                    else ""),
+                       "tokens_per_step_per_gpu": cfg.total_q,
                        "l2": "flushed (256 MB write) before every timed step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,

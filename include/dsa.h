@@ -37,7 +37,9 @@
  *   pos = L_b - T_b + i and sees keys 0..pos of its own sequence (causal,
  *   inclusive; index computation is causal, "… New-Architecture LLMs" §6.2).
  *   Prefill has T_b = L_b (pos = i); decode has T_b = 1 (pos = L_b - 1).
- *   Positions written to / read from `idx` are local to the sequence.
+ *   Positions written to / read from `idx` are local to the sequence.  The key-side
+ *   tensors (k_idx, kv, k_scale) are either packed the same way or paged through a
+ *   block table (dsa_problem.page_size, below).
  */
 #ifndef DSA_H_
 #define DSA_H_
@@ -49,7 +51,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 /* Return codes. */
 enum dsa_status {
@@ -101,6 +103,22 @@ typedef struct dsa_problem {
   float sm_scale;      /* softmax scale; 0 selects 1/sqrt(D) */
   const int32_t* cu_q; /* device int32 [B+1], cu_q[0] = 0, cu_q[B] = total_q */
   const int32_t* cu_k; /* device int32 [B+1], cu_k[0] = 0, cu_k[B] = total_k */
+  /* Paged key caches ("Day0 Inference Adaptation and Performance Optimization for
+   * New-Architecture LLMs", §4.1: the fused indexer reads the paged K cache directly; "… on
+   * Ascend", §4: the cache layout has to match the operators' addressing).  page_size = 0:
+   * the caches are packed along tokens as described above (k_idx, kv and k_scale have
+   * total_k rows, sequence b owning rows cu_k[b] .. cu_k[b+1]-1).  page_size > 0: the
+   * caches hold num_pages pages of page_size rows each (num_pages * page_size rows), and
+   * key position s of sequence b lives in cache row
+   *   block_table[b * max_pages + s / page_size] * page_size + s % page_size;
+   * cu_k then only gives the sequence lengths L_b = cu_k[b+1] - cu_k[b].  page_size must be
+   * a power of two >= 16; max_pages * page_size >= max_k_len; num_pages * page_size < 2^31.  A block-table entry outside [0, num_pages) is reported with
+   * DSA_FLAG_BAD_SEQS when the indexer reads it (those keys score 0) and with
+   * DSA_FLAG_BAD_INDEX when attention meets one of its positions (the entry is skipped). */
+  int32_t page_size;          /* 0 (contiguous) or the rows of a page */
+  int32_t max_pages;          /* pages per block-table row */
+  int32_t num_pages;          /* pages in the caches */
+  const int32_t* block_table; /* device int32 [num_seqs][max_pages], or NULL if not paged */
 } dsa_problem;
 
 /* Limits of this build: 1 <= h_idx <= 128, d_idx in {16..256, multiple of 16},

@@ -42,11 +42,23 @@ class Problem:
 
     def __init__(self, cu_q: torch.Tensor, cu_k: torch.Tensor, *, q_lens: Sequence[int],
                  k_lens: Sequence[int], h_idx: int, d_idx: int, h: int, d_c: int, d_rope: int,
-                 top_k: int, idx_dtype, kv_dtype, out_dtype=None, sm_scale: float = 0.0):
+                 top_k: int, idx_dtype, kv_dtype, out_dtype=None, sm_scale: float = 0.0,
+                 block_table: Optional[torch.Tensor] = None, page_size: int = 0,
+                 num_pages: int = 0):
+        """block_table [B, max_pages] int32 (CUDA) with page_size > 0 and num_pages: the key
+        caches (k_idx, kv, k_scale) are paged, num_pages * page_size rows; key position s of
+        sequence b is row block_table[b, s // page_size] * page_size + s % page_size."""
         if not (cu_q.is_cuda and cu_k.is_cuda) or cu_q.dtype != torch.int32 \
                 or cu_k.dtype != torch.int32:
             raise ValueError("cu_q/cu_k must be int32 CUDA tensors")
         self.cu_q, self.cu_k = cu_q.contiguous(), cu_k.contiguous()
+        self.page_size, self.num_pages = int(page_size), int(num_pages)
+        self.block_table = None
+        if self.page_size:
+            if block_table is None or not block_table.is_cuda or block_table.dtype != torch.int32 \
+                    or block_table.dim() != 2 or block_table.shape[0] != len(q_lens):
+                raise ValueError("paged caches need an int32 CUDA block_table [B, max_pages]")
+            self.block_table = block_table.contiguous()
         self.q_lens, self.k_lens = list(q_lens), list(k_lens)
         self.h_idx, self.d_idx, self.h, self.d_c, self.d_rope = h_idx, d_idx, h, d_c, d_rope
         self.top_k = top_k
@@ -56,14 +68,24 @@ class Problem:
         self.c = _abi.DsaProblem(
             len(self.q_lens), sum(self.q_lens), sum(self.k_lens), max(self.q_lens, default=0),
             max(self.k_lens), h_idx, d_idx, h, d_c, d_rope, top_k, self.idx_dtype, self.kv_dtype,
-            self.out_dtype, self.sm_scale, self.cu_q.data_ptr(), self.cu_k.data_ptr())
+            self.out_dtype, self.sm_scale, self.cu_q.data_ptr(), self.cu_k.data_ptr(),
+            self.page_size, self.block_table.shape[1] if self.page_size else 0, self.num_pages,
+            self.block_table.data_ptr() if self.page_size else None)
 
     @classmethod
-    def from_config(cls, cfg, cu_q: torch.Tensor, cu_k: torch.Tensor, sm_scale: float = 0.0):
+    def from_config(cls, cfg, cu_q: torch.Tensor, cu_k: torch.Tensor, sm_scale: float = 0.0,
+                    block_table: Optional[torch.Tensor] = None, page_size: int = 0,
+                    num_pages: int = 0):
         return cls(cu_q, cu_k, q_lens=cfg.q_lens, k_lens=cfg.k_lens, h_idx=cfg.h_idx,
                    d_idx=cfg.d_idx, h=cfg.h, d_c=cfg.d_c, d_rope=cfg.d_rope, top_k=cfg.top_k,
                    idx_dtype=cfg.idx_dtype, kv_dtype=cfg.kv_dtype, out_dtype=cfg.out_dtype,
-                   sm_scale=sm_scale)
+                   sm_scale=sm_scale, block_table=block_table, page_size=page_size,
+                   num_pages=num_pages)
+
+    @property
+    def cache_rows(self) -> int:
+        """Rows of the key caches (k_idx, kv, k_scale)."""
+        return self.num_pages * self.page_size if self.page_size else self.total_k
 
     @property
     def total_q(self) -> int:
@@ -163,11 +185,11 @@ def _need(t: Optional[torch.Tensor], name: str, dtype_code: Optional[int], shape
 
 def _check_indexer(P: Problem, q_idx, k_idx, w, q_scale, k_scale):
     _need(q_idx, "q_idx", P.idx_dtype, (P.total_q, P.h_idx, P.d_idx))
-    _need(k_idx, "k_idx", P.idx_dtype, (P.total_k, P.d_idx))
+    _need(k_idx, "k_idx", P.idx_dtype, (P.cache_rows, P.d_idx))
     _need(w, "w", _abi.DSA_F32, (P.total_q, P.h_idx))
     fp8 = P.idx_dtype == _abi.DSA_FP8_E4M3
     _need(q_scale, "q_scale", _abi.DSA_F32, (P.total_q, P.h_idx), optional=not fp8)
-    _need(k_scale, "k_scale", _abi.DSA_F32, (P.total_k,), optional=not fp8)
+    _need(k_scale, "k_scale", _abi.DSA_F32, (P.cache_rows,), optional=not fp8)
 
 
 def _idx_out(P: Problem, idx, vals, device, want_vals: bool):
@@ -234,7 +256,7 @@ def sparse_mla_attn(P: Problem, q, kv, idx, out=None, lse=None, want_lse: bool =
                     ws: Optional[Workspace] = None):
     """Sparse attention over the latent rows idx selects: (out[ΣT, H, d_c], lse or None)."""
     _need(q, "q", P.kv_dtype, (P.total_q, P.h, P.d))
-    _need(kv, "kv", P.kv_dtype, (P.total_k, P.d))
+    _need(kv, "kv", P.kv_dtype, (P.cache_rows, P.d))
     _need(idx, "idx", None, (P.total_q, P.top_k))
     dev = kv.device
     out, lse = _attn_out(P, out, lse, dev, want_lse)
@@ -251,7 +273,7 @@ def fused_forward(P: Problem, q_idx, k_idx, w, q, kv, q_scale=None, k_scale=None
     """The DSA layer: fused indexer then sparse attention → (out, lse, idx, vals)."""
     _check_indexer(P, q_idx, k_idx, w, q_scale, k_scale)
     _need(q, "q", P.kv_dtype, (P.total_q, P.h, P.d))
-    _need(kv, "kv", P.kv_dtype, (P.total_k, P.d))
+    _need(kv, "kv", P.kv_dtype, (P.cache_rows, P.d))
     dev = kv.device
     out, lse = _attn_out(P, out, lse, dev, want_lse)
     if want_idx or idx is not None:

@@ -28,7 +28,12 @@ class DsaProblem(ctypes.Structure):
                 ("d_rope", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("idx_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("sm_scale", ctypes.c_float),
-                ("cu_q", ctypes.c_void_p), ("cu_k", ctypes.c_void_p)]
+                ("cu_q", ctypes.c_void_p), ("cu_k", ctypes.c_void_p),
+                ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("block_table", ctypes.c_void_p)]
+
+
+ABI_VERSION = 2  # DSA_ABI_VERSION this binding is written for
 
 
 class DsaError(RuntimeError):
@@ -76,6 +81,9 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = ctypes.c_char_p
     L.dsa_status_str.argtypes = [ctypes.c_int]
     L.dsa_last_error.argtypes = []
+    if L.dsa_abi_version() != ABI_VERSION:
+        raise ImportError(f"{LIB_PATH} has ABI version {L.dsa_abi_version()}, the binding "
+                          f"expects {ABI_VERSION}: rebuild it")
     _lib = L
     return L
 

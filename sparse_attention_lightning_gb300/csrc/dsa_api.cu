@@ -140,6 +140,19 @@ int check_problem(const dsa_problem* p, bool need_indexer, bool need_attn) {
   if (p->top_k < 1 || p->top_k > 2048)
     return set_error(DSA_ERR_UNSUPPORTED, "top_k = %d (supported 1..2048)", p->top_k);
   if (!p->cu_q || !p->cu_k) return set_error(DSA_ERR_INVALID_ARG, "cu_q/cu_k is NULL");
+  if (p->page_size != 0) {
+    const int ps = p->page_size;
+    if (ps < 16 || (ps & (ps - 1)) != 0)
+      return set_error(DSA_ERR_UNSUPPORTED, "page_size = %d (a power of two >= 16)", ps);
+    if (!p->block_table) return set_error(DSA_ERR_INVALID_ARG, "paged caches need a block_table");
+    if (((uintptr_t)p->block_table & 15u) != 0)
+      return set_error(DSA_ERR_INVALID_ARG, "block_table is not 16-byte aligned");
+    if (p->num_pages < 1 || p->max_pages < 1 || (int64_t)p->max_pages * ps < p->max_k_len)
+      return set_error(DSA_ERR_INVALID_ARG, "num_pages = %d, max_pages = %d do not cover max_k_len",
+                       p->num_pages, p->max_pages);
+    if ((int64_t)p->num_pages * ps >= (int64_t(1) << 31))
+      return set_error(DSA_ERR_UNSUPPORTED, "num_pages * page_size >= 2^31");
+  }
   if (need_indexer) {
     if (p->h_idx < 1 || p->h_idx > 128)
       return set_error(DSA_ERR_UNSUPPORTED, "h_idx = %d (supported 1..128)", p->h_idx);
@@ -166,7 +179,14 @@ int check_problem(const dsa_problem* p, bool need_indexer, bool need_attn) {
 }
 
 Seqs seqs_of(const dsa_problem* p) {
-  return Seqs{p->cu_q, p->cu_k, p->num_seqs, p->total_q, p->total_k, p->max_k_len};
+  Seqs s{p->cu_q, p->cu_k, p->num_seqs, p->total_q, p->total_k, p->max_k_len};
+  if (p->page_size > 0) {
+    s.block_table = p->block_table;
+    s.page_size = p->page_size;
+    s.max_pages = p->max_pages;
+    s.num_pages = p->num_pages;
+  }
+  return s;
 }
 
 float scale_of(const dsa_problem* p) {

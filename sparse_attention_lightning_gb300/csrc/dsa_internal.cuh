@@ -27,6 +27,16 @@ struct Seqs {
   int total_q;
   int total_k;
   int max_k_len;
+  // Paged caches (page_size > 0): key position s of sequence b is the cache row
+  // block_table[b * max_pages + s / page_size] * page_size + s % page_size.  Otherwise
+  // the keys of sequence b are the rows cu_k[b] .. cu_k[b+1]-1.
+  const int32_t* block_table = nullptr;
+  int page_size = 0, max_pages = 0, num_pages = 0;
+  __host__ __device__ bool paged() const { return page_size > 0; }
+  // rows of the key caches (k_idx, kv, k_scale)
+  __host__ __device__ int64_t cache_rows() const {
+    return paged() ? (int64_t)num_pages * page_size : (int64_t)total_k;
+  }
 };
 
 struct RowInfo {
@@ -60,6 +70,21 @@ __device__ __forceinline__ bool query_row_info(const Seqs& s, int t, RowInfo& r,
   r.k0 = k0;
   r.L = L;
   return true;
+}
+
+// Cache row of key position `pos` of sequence b (k0 = cu_k[b]); -1 when the block table
+// points outside the cache.  (Cache rows stay below 2^31; page_size is a power of two.)
+__device__ __forceinline__ int key_row(const Seqs& s, int b, int k0, int pos) {
+  if (!s.paged()) return k0 + pos;
+  const int sh = __ffs(s.page_size) - 1;
+  const int pg = __ldg(s.block_table + (int64_t)b * s.max_pages + (pos >> sh));
+  if ((unsigned)pg >= (unsigned)s.num_pages) return -1;
+  return (pg << sh) | (pos & (s.page_size - 1));
+}
+
+// Rows a 128-key tile is loaded in: a paged tile comes page by page.
+__host__ __device__ __forceinline__ int tile_chunk_rows(const Seqs& s) {
+  return s.paged() && s.page_size < 128 ? s.page_size : 128;
 }
 
 // ----------------------------------------------------------------------------

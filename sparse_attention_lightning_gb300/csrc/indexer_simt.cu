@@ -59,8 +59,13 @@ indexer_scores_simt_kernel(IndexerArgs a, float* __restrict__ scores, int64_t ld
       const int64_t s = s0 + kr;
       float v = 0.f;
       if (s <= r.pos) {
-        v = to_f32(kg[(r.k0 + s) * DI + c]);
-        if (fp8) v *= __ldg(a.k_scale + r.k0 + s);
+        const int64_t row = (int64_t)key_row(a.seqs, r.b, r.k0, (int)s);  // -1: page outside the cache
+        if (row >= 0) {
+          v = to_f32(kg[row * DI + c]);
+          if (fp8) v *= __ldg(a.k_scale + row);
+        } else if (c == 0) {
+          atomicOr(a.status, DSA_FLAG_BAD_SEQS);
+        }
       }
       ks[kr * (DI + 1) + c] = v;
     }

@@ -242,19 +242,36 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (!mbar_wait(&k_empty[s], ((it / C::NS) & 1) ^ 1, abort_flag, p.status,
                        DSA_FLAG_TIMEOUT)) break;
         const int key0 = cur.k0 + cur.j * C::BM;
+        float* sdst = scs + (it % NSCM) * (C::SC_SLOT / 4);
         if (FP8) {
           // the tile's key scales land with its keys (the MMA waits for both)
           const int sl = it % NSCM;
           if (!mbar_wait(&sc_empty[sl], ((it / NSCM) & 1) ^ 1, abort_flag, p.status,
                          DSA_FLAG_TIMEOUT)) break;
-          mbar_arrive_expect_tx(&k_full[s], C::KTILE + C::SC_BYTES);
-          tma_load_2d(scs + sl * (C::SC_SLOT / 4), &smap, &k_full[s], key0 & ~3, 0);
+          mbar_arrive_expect_tx(&k_full[s], C::KTILE + (p.seqs.paged() ? C::BM * 4 : C::SC_BYTES));
         } else {
           mbar_arrive_expect_tx(&k_full[s], C::KTILE);
         }
-        for (int a = 0; a < C::ATOMS; ++a)
-          tma_load_2d_hint(ks + s * C::KTILE + a * (C::BM * 128), &kmap, &k_full[s],
-                           a * (128 / C::ES), key0, pol);
+        if (!p.seqs.paged()) {
+          if (FP8) tma_load_2d(sdst, &smap, &k_full[s], key0 & ~3, 0);
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_2d_hint(ks + s * C::KTILE + a * (C::BM * 128), &kmap, &k_full[s],
+                             a * (128 / C::ES), key0, pol);
+        } else {
+          // page by page: chunks of cr rows; a chunk past the block's history or on a page
+          // outside the cache is read out of bounds (zero fill) and never stored
+          const int cr = tile_chunk_rows(p.seqs);
+          const int s0 = cur.j * C::BM, nk = cur.pos + cur.nrow;
+          for (int q = 0; q < C::BM / cr; ++q) {
+            int64_t row = s0 + q * cr < nk ? key_row(p.seqs, cur.b, cur.k0, s0 + q * cr) : -2;
+            if (row == -1) atomicOr(p.status, DSA_FLAG_BAD_SEQS);
+            if (row < 0) row = p.seqs.cache_rows();
+            if (FP8) tma_load_2d(sdst + q * cr, &smap, &k_full[s], (int)row, 0);
+            for (int a = 0; a < C::ATOMS; ++a)
+              tma_load_2d_hint(ks + s * C::KTILE + a * (C::BM * 128) + q * cr * 128, &kmap,
+                               &k_full[s], a * (128 / C::ES), (int)row, pol);
+          }
+        }
         issued = it + 1;
       }
       // every copy issued has landed before the CTA may exit
@@ -348,8 +365,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // this thread's key scale, landed with the tile (its MMA waited for both); keys past
         // the block read a neighbour's scale or the zero fill, and are not stored
         const int sl = it % NSCM;
-        const int key0 = cur.k0 + cur.j * C::BM;
-        ksc = scs[sl * (C::SC_SLOT / 4) + (key0 & 3) + quarter * 32 + lane];
+        const int sh = p.seqs.paged() ? 0 : ((cur.k0 + cur.j * C::BM) & 3);
+        ksc = scs[sl * (C::SC_SLOT / 4) + sh + quarter * 32 + lane];
         __syncwarp();
         if (lane == 0) mbar_arrive(&sc_empty[sl]);
       }
@@ -439,16 +456,19 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
   using C = Cfg<FP8, QB>;
   CUtensorMap kmap, qmap, smap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  int rc = make_tmap_2d(&kmap, dt, a.k_idx, C::DI, (uint64_t)a.seqs.total_k, C::ROWB,
-                        128 / C::ES, C::BM);
+  const int cr = tile_chunk_rows(a.seqs);  // key rows per copy (a page, for small pages)
+  int rc = make_tmap_2d(&kmap, dt, a.k_idx, C::DI, (uint64_t)a.seqs.cache_rows(), C::ROWB,
+                        128 / C::ES, (uint32_t)cr);
   if (rc != DSA_OK) return rc;
   rc = make_tmap_2d(&qmap, dt, a.q_idx, C::DI, (uint64_t)a.seqs.total_q * C::HI, C::ROWB,
                     128 / C::ES, C::N);
   if (rc != DSA_OK) return rc;
   if (FP8) {
     // k_scale as one row of total_k floats (no swizzle), read in boxes of 132
-    rc = make_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, (uint64_t)a.seqs.total_k,
-                      1, align_up((size_t)a.seqs.total_k * 4, 16), C::SC_BOX, 1, false);
+    const uint64_t rows = (uint64_t)a.seqs.cache_rows();
+    rc = make_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, rows, 1,
+                      align_up((size_t)rows * 4, 16), a.seqs.paged() ? (uint32_t)cr : C::SC_BOX,
+                      1, false);
     if (rc != DSA_OK) return rc;
   } else {
     smap = kmap;  // unused

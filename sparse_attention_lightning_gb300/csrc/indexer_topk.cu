@@ -84,7 +84,9 @@ struct Cfg {
   static constexpr int OFF_A3 = OFF_A2 + kNB2 * 4;            // round 3
   static constexpr int OFF_CNT = OFF_A3 + kNB3 * 4;           // per (tile, quarter) counts
   static constexpr int OFF_SC = OFF_CNT + kMaxTiles * 4 * 4;  // FP8 scale ring
-  static constexpr int OFF_MISC = OFF_SC + NSC * SC_SLOT;
+  static constexpr int OFF_PG = OFF_SC + NSC * SC_SLOT;       // the CTA's pages (paged caches)
+  static constexpr int MAX_PG = kMaxTiles * (kBM / 16);       // 16-row pages at most
+  static constexpr int OFF_MISC = OFF_PG + MAX_PG * 4;
   static constexpr int MISC = 1024;
   static constexpr int SMEM = OFF_MISC + MISC + 1024 /*alignment*/;
   static_assert(SMEM <= 232448, "shared memory");
@@ -205,6 +207,7 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   uint32_t* A3 = reinterpret_cast<uint32_t*>(smem + C::OFF_A3);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + C::OFF_CNT);
   float* scs = reinterpret_cast<float*>(smem + C::OFF_SC);
+  int32_t* pages = reinterpret_cast<int32_t*>(smem + C::OFF_PG);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
   uint64_t* k_full = bars;                   // [NSS]
   uint64_t* k_empty = k_full + C::NSS;       // [NSS]
@@ -254,6 +257,15 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     if (FP8) prefetch_tmap(&smap);
   }
   for (int i = threadIdx.x; i < kNB1; i += kThreads) { h[i] = 0u; A1[i] = 0u; }
+  // paged caches: the block-table entries of this CTA's keys, fetched once (the producer
+  // would otherwise wait for each lookup before it can issue the copy)
+  const int cr = tile_chunk_rows(p.seqs);
+  const int pg0 = p.seqs.paged() ? j0 * kBM / p.seqs.page_size : 0;  // first page of the CTA
+  if (p.seqs.paged() && stream) {
+    const int npg = min((min(j1 * kBM, n) - 1) / p.seqs.page_size - pg0 + 1, C::MAX_PG);
+    for (int i = threadIdx.x; i < npg; i += kThreads)
+      pages[i] = __ldg(p.seqs.block_table + (int64_t)ri.b * p.seqs.max_pages + pg0 + i);
+  }
   for (int i = threadIdx.x; i < kNB2; i += kThreads) A2[i] = 0u;
   for (int i = threadIdx.x; i < kNB3; i += kThreads) A3[i] = 0u;
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
@@ -272,6 +284,7 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     if (warp == 0) {
       // ---- TMA producer: pair p = tiles 2p, 2p + 1 into stage p % NSS ----
       if (lane == 0) {
+        const int sc_bytes = p.seqs.paged() ? kBM * 4 : C::SC_BYTES;
         const uint64_t pol = l2_policy_evict_first();
         int issued = 0;
         mbar_arrive_expect_tx(q_full, C::QTILE);
@@ -290,15 +303,37 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                              DSA_FLAG_TIMEOUT);
             }
           if (!ok) break;
-          mbar_arrive_expect_tx(&k_full[ss], nt * (C::KTILE + (FP8 ? C::SC_BYTES : 0)));
+          mbar_arrive_expect_tx(&k_full[ss], nt * (C::KTILE + (FP8 ? sc_bytes : 0)));
           for (int j = 0; j < nt; ++j) {
             const int it = kPair * pp + j;
-            const int key0 = ri.k0 + (j0 + it) * kBM;
-            if (FP8)
-              tma_load_2d(scs + (it % NSCM) * (C::SC_SLOT / 4), &smap, &k_full[ss], key0 & ~3, 0);
-            for (int a = 0; a < C::ATOMS; ++a)
-              tma_load_2d_hint(ks + ss * C::STAGE + j * C::KTILE + a * (kBM * 128), &kmap,
-                               &k_full[ss], a * (128 / C::ES), key0, pol);
+            const int s0 = (j0 + it) * kBM;  // the tile's first key position
+            uint8_t* kdst = ks + ss * C::STAGE + j * C::KTILE;
+            float* sdst = scs + (it % NSCM) * (C::SC_SLOT / 4);
+            if (!p.seqs.paged()) {
+              const int key0 = ri.k0 + s0;
+              if (FP8) tma_load_2d(sdst, &smap, &k_full[ss], key0 & ~3, 0);
+              for (int a = 0; a < C::ATOMS; ++a)
+                tma_load_2d_hint(kdst + a * (kBM * 128), &kmap, &k_full[ss], a * (128 / C::ES),
+                                 key0, pol);
+            } else {
+              // page by page: chunks of cr rows; a chunk past the history or on a page outside
+              // the cache is read out of bounds (zero fill) and never selected
+              for (int q = 0; q < kBM / cr; ++q) {
+                const int pos = s0 + q * cr;
+                int64_t row = -2;
+                if (pos < n) {
+                  const int pg = pages[pos / p.seqs.page_size - pg0];
+                  row = pg >= 0 && pg < p.seqs.num_pages
+                            ? (int64_t)pg * p.seqs.page_size + pos % p.seqs.page_size : -1;
+                }
+                if (row == -1) atomicOr(p.status, DSA_FLAG_BAD_SEQS);
+                if (row < 0) row = p.seqs.cache_rows();
+                if (FP8) tma_load_2d(sdst + q * cr, &smap, &k_full[ss], (int)row, 0);
+                for (int a = 0; a < C::ATOMS; ++a)
+                  tma_load_2d_hint(kdst + a * (kBM * 128) + q * cr * 128, &kmap, &k_full[ss],
+                                   a * (128 / C::ES), (int)row, pol);
+              }
+            }
           }
           issued = pp + 1;
         }
@@ -368,8 +403,8 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             // this thread's key scale, landed with the tile; keys past the row read a
             // neighbour's scale or the zero fill and are never selected
             const int sl = it % NSCM;
-            const int key0 = ri.k0 + (j0 + it) * kBM;
-            ksc = scs[sl * (C::SC_SLOT / 4) + (key0 & 3) + quarter * 32 + lane];
+            const int sh = p.seqs.paged() ? 0 : ((ri.k0 + (j0 + it) * kBM) & 3);
+            ksc = scs[sl * (C::SC_SLOT / 4) + sh + quarter * 32 + lane];
             __syncwarp();
             if (lane == 0) mbar_arrive(&sc_empty[sl]);
           }
@@ -640,13 +675,17 @@ int launch_typed(const IndexerArgs& a, int top_k, int32_t* idx, float* vals, cud
   using C = Cfg<FP8>;
   CUtensorMap kmap, qmap, smap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  int rc = make_tmap_2d(&kmap, dt, a.k_idx, kDI, (uint64_t)a.seqs.total_k, C::ROWB, 128 / C::ES, kBM);
+  const int cr = tile_chunk_rows(a.seqs);  // key rows per copy (a page, for small pages)
+  int rc = make_tmap_2d(&kmap, dt, a.k_idx, kDI, (uint64_t)a.seqs.cache_rows(), C::ROWB, 128 / C::ES,
+                        (uint32_t)cr);
   if (rc != DSA_OK) return rc;
   rc = make_tmap_2d(&qmap, dt, a.q_idx, kDI, (uint64_t)a.seqs.total_q * kHI, C::ROWB, 128 / C::ES, kHI);
   if (rc != DSA_OK) return rc;
   if (FP8) {
-    rc = make_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, (uint64_t)a.seqs.total_k, 1,
-                      align_up((size_t)a.seqs.total_k * 4, 16), C::SC_BOX, 1, false);
+    const uint64_t rows = (uint64_t)a.seqs.cache_rows();
+    rc = make_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, rows, 1,
+                      align_up((size_t)rows * 4, 16), a.seqs.paged() ? (uint32_t)cr : C::SC_BOX,
+                      1, false);
     if (rc != DSA_OK) return rc;
   } else {
     smap = kmap;  // unused
@@ -677,11 +716,15 @@ int launch_typed(const IndexerArgs& a, int top_k, int32_t* idx, float* vals, cud
 
 }  // namespace
 
+// Rows whose clusters all fit on the GPU at once (one CTA per SM): several waves would each
+// end in a selection tail with their SMs idle, and the persistent indexer, which keeps every
+// SM streaming to the end, followed by the streaming Top-K is faster there.
 bool indexer_topk_eligible(const IndexerArgs& a) {
   const int64_t ntiles = ((int64_t)a.seqs.max_k_len + kBM - 1) / kBM;
+  const int64_t c_cap = (ntiles + kMaxTiles - 1) / kMaxTiles;
   return (a.idx_dtype == DSA_BF16 || a.idx_dtype == DSA_FP8_E4M3) && a.h_idx == kHI &&
-         a.d_idx == kDI && ntiles <= (int64_t)kMaxCluster * kMaxTiles &&
-         (int64_t)a.seqs.total_q * kMaxCluster < (int64_t(1) << 31) &&
+         a.d_idx == kDI && c_cap <= kMaxCluster &&
+         (int64_t)a.seqs.total_q * c_cap <= num_sms() &&
          (a.idx_dtype != DSA_FP8_E4M3 || (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0);
 }
 

@@ -90,7 +90,13 @@ extern "C" int dsa_fused_indexer_static(const dsa_problem* p, const void* q_idx,
 
   cudaError_t e = cudaMemsetAsync(status, 0, kStatusBytes, s);
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "clear status: %s", cudaGetErrorString(e));
-  const Seqs seqs{p->cu_q, p->cu_k, p->num_seqs, p->total_q, p->total_k, p->max_k_len};
+  Seqs seqs{p->cu_q, p->cu_k, p->num_seqs, p->total_q, p->total_k, p->max_k_len};
+  if (p->page_size > 0) {  // paged key caches (checked by dsa_workspace_size above)
+    seqs.block_table = p->block_table;
+    seqs.page_size = p->page_size;
+    seqs.max_pages = p->max_pages;
+    seqs.num_pages = p->num_pages;
+  }
   IndexerArgs ia{seqs, p->h_idx, p->d_idx, p->idx_dtype, q_idx, k_idx, w,
                  fp8 ? q_scale : nullptr, fp8 ? k_scale : nullptr, status};
   rc = launch_indexer_scores_simt(ia, scores, p->max_k_len, s);

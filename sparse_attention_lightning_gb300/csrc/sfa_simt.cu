@@ -49,9 +49,14 @@ __global__ void __launch_bounds__(kThreads) sfa_simt_kernel(SfaArgs a) {
     const int i = base + tid;
     int v = -1;
     bool ok = false;
+    int64_t row = -1;
     if (i < a.top_k) {
       v = irow[i];
       ok = (v >= 0 && v <= r.pos);
+      if (ok) {
+        row = key_row(a.seqs, r.b, r.k0, v);  // -1: page outside the cache
+        ok = row >= 0;
+      }
       if (!ok && v != -1) atomicOr(a.status, DSA_FLAG_BAD_INDEX);
     }
     const unsigned bal = __ballot_sync(0xffffffffu, ok);
@@ -60,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) sfa_simt_kernel(SfaArgs a) {
     __syncthreads();
     int off = s_nvalid;
     for (int w = 0; w < warp; ++w) off += warp_cnt[w];
-    if (ok) sel[off + __popc(bal & ((1u << lane) - 1u))] = r.k0 + v;
+    if (ok) sel[off + __popc(bal & ((1u << lane) - 1u))] = (int32_t)row;
     __syncthreads();
     if (tid == 0) {
       int tot = 0;

@@ -103,7 +103,7 @@ struct Params {
   float* lse;
   float4* part_o;    // [(total_q + clusters - 1) * 2][64][128] float4 (pieces)
   float* part_ml;    // [(total_q + clusters - 1) * 2][128][2]
-  int32_t* lists;    // [gridDim.x][kMaxTopK]: each CTA's compacted key rows of its unit
+  int32_t* lists;    // [gridDim.x][kMaxTopK]: each CTA's compacted cache rows of its unit
   uint32_t* status;
 };
 
@@ -196,6 +196,9 @@ __device__ __forceinline__ void row_pieces(const Params& p, int t, int ncl, int&
   np = share_of(p, (int64_t)(t + 1) * p.C - 1, ncl) - cf + 1;
 }
 
+// PAGED: key rows through the block table (a separate instantiation, so that the packed
+// layout's index compaction stays as short as it is without paging).
+template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 sfa_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -289,13 +292,27 @@ sfa_tc_kernel(Params p) {
 #pragma unroll
         for (int j = 0; j < kMaxTopK / 32; ++j)
           v[j] = (ok && j < seg && s0 + j < len) ? __ldg(irow + s0 + j) : -1;
+        // valid entries: in [0, pos] (and, paged, on a page inside the cache; those become
+        // their cache rows here, the others -1)
         int cnt = 0;
         bool bad = false;
+        if (!PAGED) {
 #pragma unroll
-        for (int j = 0; j < kMaxTopK / 32; ++j) {
-          const bool valid = v[j] >= 0 && v[j] <= pos;
-          bad |= !valid && v[j] != -1;
-          cnt += valid;
+          for (int j = 0; j < kMaxTopK / 32; ++j) {
+            const bool valid = v[j] >= 0 && v[j] <= pos;
+            bad |= !valid && v[j] != -1;
+            cnt += valid;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kMaxTopK / 32; ++j) {
+            const bool in_range = v[j] >= 0 && v[j] <= pos;
+            const int row = in_range ? key_row(p.seqs, b, k0, v[j]) : -1;
+            const bool valid = row >= 0;
+            bad |= !valid && v[j] != -1;
+            v[j] = valid ? row : -1;
+            cnt += valid;
+          }
         }
         if (bad && rank == 0) atomicOr(p.status, DSA_FLAG_BAD_INDEX);
         int before = cnt;
@@ -310,9 +327,15 @@ sfa_tc_kernel(Params p) {
         if (!__all_sync(0xffffffffu, mbar_wait(meta_empty, (ui & 1) ^ 1, abort_flag, p.status,
                                                DSA_FLAG_TIMEOUT)))
           break;
+        if (!PAGED) {
 #pragma unroll
-        for (int j = 0; j < kMaxTopK / 32; ++j)
-          if (v[j] >= 0 && v[j] <= pos) list[before++] = k0 + v[j];
+          for (int j = 0; j < kMaxTopK / 32; ++j)
+            if (v[j] >= 0 && v[j] <= pos) list[before++] = k0 + v[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < kMaxTopK / 32; ++j)
+            if (v[j] >= 0) list[before++] = v[j];
+        }
         __syncwarp();
         if (lane == 0) { *meta_nv = nv; mbar_arrive(meta_full); }
       } else {
@@ -864,7 +887,8 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
     b += align_up(slots * kH * 256 * 4, 256);
     p.part_ml = reinterpret_cast<float*>(b);
   }
-  if (cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+  auto kern = a.seqs.paged() ? sfa_tc_kernel<true> : sfa_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return check_launch("sfa_tc: smem attribute");
   const int64_t units = pieces ? p.tot : (int64_t)a.seqs.total_q;
@@ -876,7 +900,7 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   p.nclusters = clusters;
   cudaError_t e = cudaSuccess;
   DSA_LAUNCH("sfa_tc", stream,
-             e = launch_pdl(sfa_tc_kernel, dim3(2 * clusters), dim3(kThreads), kSmem, stream, p));
+             e = launch_pdl(kern, dim3(2 * clusters), dim3(kThreads), kSmem, stream, p));
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
   int rc = check_launch("sfa_tc");
   if (rc != DSA_OK || !pieces) return rc;

@@ -213,3 +213,65 @@ def custom(q_lens, k_lens, h_idx=4, d_idx=32, h=8, d_c=64, d_rope=16, top_k=32,
            idx_dtype=F32, kv_dtype=F32, out_dtype=None, name="custom") -> Config:
     return Config(name, list(q_lens), list(k_lens), h_idx, d_idx, h, d_c, d_rope, top_k,
                   idx_dtype, kv_dtype, out_dtype or kv_dtype)
+
+
+# ---------------------------------------------------------------------------
+# Paged key caches: the same key-side rows scattered over pages.
+
+_PAGE_STREAM = 7
+
+
+@dataclasses.dataclass
+class PagedKeys:
+    """Key-side tensors of a case laid out in pages, and the block table that maps them."""
+
+    page_size: int
+    num_pages: int
+    block_table: torch.Tensor   # int32 [B, max_pages]: page of each sequence's page slot, -1 unused
+    k_idx: torch.Tensor         # [num_pages * page_size, d_I]
+    kv: torch.Tensor            # [num_pages * page_size, D]
+    k_scale: Optional[torch.Tensor] = None  # f32 [num_pages * page_size] (FP8 only)
+
+    def tensors(self) -> Dict[str, torch.Tensor]:
+        out = {"block_table": self.block_table, "k_idx": self.k_idx, "kv": self.kv}
+        if self.k_scale is not None:
+            out["k_scale"] = self.k_scale
+        return out
+
+
+def paged_keys(case: Case, page_size: int, seed: int, spare_pages: int = 3) -> PagedKeys:
+    """Scatter the key side of ``case`` over pages: sequence b's L_b keys fill
+    ceil(L_b / page_size) pages, drawn in a seeded random order from a pool that also holds
+    ``spare_pages`` unused pages.  Rows that hold no key (unused pages, page tails) are
+    filled with large values, so that reading one shows up in the results."""
+    lens = list(case.cfg.k_lens)
+    need = [(L + page_size - 1) // page_size for L in lens]
+    num_pages = sum(need) + spare_pages
+    max_pages = max(max(need), 1)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) * 1_000_003 + _PAGE_STREAM)
+    order = torch.randperm(num_pages, generator=g)
+    table = torch.full((len(lens), max_pages), -1, dtype=torch.int32)
+    rows = num_pages * page_size
+    src = torch.full((rows,), -1, dtype=torch.int64)  # packed key row held by each cache row
+    nxt, k0 = 0, 0
+    for b, (L, npg) in enumerate(zip(lens, need)):
+        for i in range(npg):
+            pg = int(order[nxt])
+            nxt += 1
+            table[b, i] = pg
+            n = min(page_size, L - i * page_size)
+            src[pg * page_size: pg * page_size + n] = torch.arange(k0 + i * page_size,
+                                                                   k0 + i * page_size + n)
+        k0 += L
+    used = src >= 0
+
+    def scatter(x: torch.Tensor, fill) -> torch.Tensor:
+        out = torch.full((rows,) + tuple(x.shape[1:]), fill, dtype=x.dtype)
+        out[used] = x[src[used]]
+        return out
+
+    fill_idx = 0x7E if case.k_idx.dtype == torch.uint8 else 100.0  # E4M3 code 0x7E = 448
+    k_scale = scatter(case.k_scale, 1.0e4) if case.k_scale is not None else None
+    return PagedKeys(page_size, num_pages, table, scatter(case.k_idx, fill_idx),
+                     scatter(case.kv, 100.0), k_scale)

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
     assert names == set(_abi.EXPORTS), names ^ set(_abi.EXPORTS)
     for n in names:
         assert hasattr(L, n), n
-    assert L.dsa_abi_version() == 1
+    assert L.dsa_abi_version() == _abi.ABI_VERSION == 2
 
 
 def _problem(**kw):
@@ -70,6 +70,27 @@ def test_descriptor_checks(L, field, value, code):
     p = _problem(**{field: value})
     assert _ws_size(L, p, _abi.OP_FUSED_FORWARD)[0] == code
     assert L.dsa_last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page_size=48, max_pages=2, num_pages=4, block_table=1 << 16), _abi.DSA_ERR_UNSUPPORTED),
+    (dict(page_size=384, max_pages=1, num_pages=4, block_table=1 << 16), _abi.DSA_ERR_UNSUPPORTED),
+    (dict(page_size=64, max_pages=1, num_pages=4, block_table=None), _abi.DSA_ERR_INVALID_ARG),
+    (dict(page_size=64, max_pages=1, num_pages=4, block_table=(1 << 16) + 4),
+     _abi.DSA_ERR_INVALID_ARG),
+    (dict(page_size=16, max_pages=3, num_pages=4, block_table=1 << 16), _abi.DSA_ERR_INVALID_ARG),
+    (dict(page_size=128, max_pages=1, num_pages=0, block_table=1 << 16), _abi.DSA_ERR_INVALID_ARG),
+    (dict(page_size=1 << 14, max_pages=1, num_pages=1 << 17, block_table=1 << 16),
+     _abi.DSA_ERR_UNSUPPORTED),
+])
+def test_paged_descriptor_checks(L, kw, code):
+    # page sizes: powers of two >= 16; the block table must exist, be aligned and
+    # cover max_k_len (64 keys here); the cache must stay below 2^31 rows
+    p = _problem(**kw)
+    assert _ws_size(L, p, _abi.OP_FUSED_FORWARD)[0] == code
+    assert L.dsa_last_error()
+    ok = _problem(page_size=32, max_pages=2, num_pages=3, block_table=1 << 16)
+    assert _ws_size(L, ok, _abi.OP_FUSED_FORWARD)[0] == _abi.DSA_OK
 
 
 def test_pointer_and_workspace_checks_launch_nothing(L):

@@ -311,3 +311,69 @@ def test_fp8_decode_workload_first_sequences():
     case = W.make_case(cfg, W.WORKLOAD_SEEDS["fp8_decode"])
     P, out, lse, idx, vals = run_fused(case)
     check_rows(case, idx, vals, out, lse, range(cfg.total_q))
+
+
+BIG = dict(h_idx=64, d_idx=128, h=128, d_c=512, d_rope=64, top_k=2048)
+PAGED = [
+    # decode rows (the one-kernel fused indexer) with pages smaller than, equal to and
+    # larger than the 128-key tile
+    ([1, 1, 1], [3000, 700, 5000], BIG, ("bf16", "bf16"), 64),
+    ([1, 1, 1], [3000, 700, 5000], BIG, ("bf16", "bf16"), 16),
+    ([1, 1, 1], [3000, 700, 5000], BIG, ("e4m3", "bf16"), 256),
+    # several queries per sequence: the persistent indexer on blocks of four rows, row
+    # chunks selected by the streaming Top-K
+    ([37, 1, 130, 6], [300, 2500, 1300, 6], dict(BIG, top_k=256), ("bf16", "bf16"), 128),
+    ([37, 1, 130, 6], [300, 2500, 1300, 6], dict(BIG, top_k=256), ("e4m3", "bf16"), 32),
+    # the CUDA-core paths (fp32, small heads)
+    ([1, 7, 40, 1], [1, 300, 40, 2049], dict(top_k=32), ("f32", "f32"), 16),
+]
+
+
+@pytest.mark.parametrize("qs,ks,dims,dts,page_size", PAGED)
+def test_paged_caches_match_oracle(qs, ks, dims, dts, page_size):
+    """The key side scattered over pages in a random order (unused rows hold large values),
+    read through the block table; every row checked against the oracle of the packed case."""
+    cfg = W.custom(qs, ks, idx_dtype=dts[0], kv_dtype=dts[1], **dims)
+    case = W.make_case(cfg, seed=11)
+    pk = W.paged_keys(case, page_size, seed=12)
+    d = to_dev(case)
+    d.update({k: v.cuda() for k, v in pk.tensors().items()})
+    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"], block_table=d["block_table"],
+                                page_size=page_size, num_pages=pk.num_pages)
+    ws = dsa.Workspace()
+    ws.clear_status()
+    out, lse, idx, vals = dsa.fused_forward(P, d["q_idx"], d["k_idx"], d["w"], d["q"], d["kv"],
+                                            d.get("q_scale"), d.get("k_scale"), want_vals=True,
+                                            ws=ws)
+    assert ws.status() == 0
+    check_rows(case, idx, vals, out, lse, range(cfg.total_q))
+    if cfg.idx_dtype != "f32":
+        # the materialised scores read the pages the same way
+        s = dsa.indexer_scores(P, d["q_idx"], d["k_idx"], d["w"], d.get("q_scale"),
+                               d.get("k_scale"))
+        torch.cuda.synchronize()
+        p = O.problem_from_case(case)
+        sn = to_np(s)
+        for t in range(cfg.total_q):
+            check_scores_row(sn[t], p.scores(t), f"paged scores row {t}")
+
+
+@pytest.mark.parametrize("top_k,flag", [(256, 0x2), (2048, 0x1)],
+                         ids=["indexer_reads_it", "every_key_kept"])
+def test_paged_block_table_outside_cache_is_flagged(top_k, flag):
+    # a block-table entry past the cache: the indexer reports it when it scores the row
+    # (DSA_FLAG_BAD_SEQS); when the row keeps every key (k >= L) the indexer reads no key and
+    # attention reports the entries it skips (DSA_FLAG_BAD_INDEX)
+    cfg = W.custom([1, 1], [700, 300], idx_dtype="bf16", kv_dtype="bf16", **dict(BIG, top_k=top_k))
+    case = W.make_case(cfg, seed=13)
+    pk = W.paged_keys(case, 64, seed=14)
+    bt = pk.block_table.clone()
+    bt[1, 2] = pk.num_pages + 5          # a page that does not exist
+    d = to_dev(case)
+    d.update({k: v.cuda() for k, v in pk.tensors().items()})
+    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"], block_table=bt.cuda(),
+                                page_size=64, num_pages=pk.num_pages)
+    ws = dsa.Workspace()
+    ws.clear_status()
+    dsa.fused_forward(P, d["q_idx"], d["k_idx"], d["w"], d["q"], d["kv"], ws=ws)
+    assert ws.status() & flag, f"flag {flag:#x} not set"
