@@ -233,12 +233,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="profiling: keep only the workload's first N sequences (same shapes)")
+    ap.add_argument("--extra", default="prefill_8k,fp8_decode,prefill_64k",
+                    help="other workloads timed after the primary one (N=1 only), reported "
+                         "under \"workloads\"; empty for none")
     ap.add_argument("--page-size", type=int, default=0,
                     help="read the key caches through a block table of pages of this many rows "
                          "(pages in a seeded random order)")
     args = ap.parse_args()
     if args.impl == "reference":
         os.environ.setdefault("OPENBLAS_NUM_THREADS", str(cores()))
+    if args.batch or args.page_size:
+        args.extra = ""
 
     import torch
     import torch.distributed as dist
@@ -272,107 +277,14 @@ def main():
     import sparse_attention_lightning_gb300 as dsa
     dsa.lib()
 
-    case = W.make_case(cfg, seed)
-    d = {k: v.to(dev) for k, v in case.tensors().items()}
-    paging = {}
-    if args.page_size:
-        pk = W.paged_keys(case, args.page_size, seed)
-        d.update({k: v.to(dev) for k, v in pk.tensors().items()})
-        paging = dict(block_table=d["block_table"], page_size=args.page_size,
-                      num_pages=pk.num_pages)
-    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"], **paging)
-    ws = dsa.Workspace(dev, P.workspace_size(5))
-    out = torch.empty(cfg.total_q, cfg.h, cfg.d_c, dtype=torch.bfloat16 if cfg.out_dtype == "bf16"
-                      else torch.float32, device=dev)
-    lse = torch.empty(cfg.total_q, cfg.h, dtype=torch.float32, device=dev)
-    idx = torch.empty(cfg.total_q, cfg.top_k, dtype=torch.int32, device=dev)
-
-    def step():
-        dsa.fused_forward(P, d["q_idx"], d["k_idx"], d["w"], d["q"], d["kv"], d.get("q_scale"),
-                          d.get("k_scale"), out=out, lse=lse, idx=idx, ws=ws)
-
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
-    ws.clear_status()
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    flags = ws.status()
-    if flags:
-        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    # timed steps: no per-kernel events in the stream, so each kernel may start while the
-    # one before it finishes (programmatic dependent launch)
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            evs[i][0].record()
-            step()
-            evs[i][1].record()
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    # a second pass of the same steps with CUDA events around every launch (on its stream):
-    # per-kernel durations for the roofline and the launch count
-    with dsa.trace(capacity=64 * args.steps) as tr:
-        for i in range(args.steps):
-            flush.zero_()
-            step()
-        torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    total_ms = float(t_max.item())
+    run = setup(dsa, W, cfg, seed, dev, args.page_size)
+    case, d, P, ws, out, lse, idx, step = run
+    res = time_steps(dsa, torch, dist, step, ws, dev, args.steps, args.warmup, world, local)
+    step_ms, total_ms, records, clocks = res
     tokens = cfg.total_q * args.steps * world
     value = tokens / (total_ms / 1e3)
-
-    # per-kernel times (CUDA events around each launch, on its stream)
-    per_kernel = {}
-    for name, ms in tr.records:
-        per_kernel.setdefault(name, []).append(ms)
-    model = work_model(cfg)
-    peaks, peak_src = load_peaks()
-    dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
-    dom_ms = statistics.mean(per_kernel[dom])
-    stage = KERNEL_STAGE.get(dom, dom)
-    decode_like = max(cfg.q_lens) == 1
-    if decode_like or stage == "topk":
-        alg = model[stage]["bytes"] if stage in model else cfg.total_q * cfg.top_k * 4
-        achieved = alg / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"],
-                "traffic": measured_traffic(dom, args.workload if not args.batch else None), "kernel": dom,
-                "algorithmic_bytes_per_launch": alg, "peak_source": f"{peak_src} hbm_gbs"}
-    else:
-        alg = model[stage]["flops"]
-        achieved = alg / (dom_ms / 1e3) / 1e12
-        pk = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": measured_traffic(dom, args.workload if not args.batch else None),
-                "kernel": dom,
-                "algorithmic_flops_per_launch": alg, "peak_source": f"{peak_src} bf16_tflops"}
-    roof["kernel_ms_mean"] = dom_ms
-    kernels = {k: {"launches": len(v), "ms_mean": statistics.mean(v),
-                   "share": sum(v) / sum(sum(x) for x in per_kernel.values())}
-               for k, v in per_kernel.items()}
-    # every kernel against its own bound: bytes for decode and Top-K, flops otherwise
-    for k, v in kernels.items():
-        st = KERNEL_STAGE.get(k)
-        if st not in model:
-            continue
-        if decode_like or st == "topk":
-            ach = model[st]["bytes"] / (v["ms_mean"] / 1e3) / 1e9
-            v.update(achieved=ach, unit="GB/s", frac=ach / peaks["hbm_gbs"])
-        else:
-            ach = model[st]["flops"] / (v["ms_mean"] / 1e3) / 1e12
-            v.update(achieved=ach, unit="TFLOP/s", frac=ach / peaks["bf16_tflops"])
+    roof, kernels = roofline(cfg, records, args.workload if not (args.batch or args.page_size)
+                             else None, args.steps)
 
     # end to end through the public API: per-step inputs from pinned host memory, result back.
     # A serving loop overlaps transfers with compute: step i's inputs are copied in (copy-in
@@ -446,8 +358,31 @@ def main():
         n, el, passes = oracle_baseline(case)
         cpu = {"value": n / el, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
                "sample": f"{n} query rows of this workload ({passes} pass(es) over its "
-                         f"{cfg.total_q} rows), fp64 numpy, BLAS threads = default",
-               "seconds": el}
+                         f"{cfg.total_q} rows), fp64 numpy on all {cores()} cores (BLAS "
+                         f"threads); one_core: the same oracle with one BLAS thread",
+               "seconds": el, "one_core": one_core_baseline(args.workload)}
+
+    # the other workloads of the metric (prefill and FP8-indexer decode): each its own
+    # timed steps, per-kernel roofline and clocks, on the same GPU after the primary one
+    extra = {}
+    if world == 1 and args.extra:
+        del run, case, d, P, ws, out, lse, idx, step
+        torch.cuda.empty_cache()
+        for name in [x for x in args.extra.split(",") if x and x != args.workload]:
+            ecfg = W.workload(name)
+            erun = setup(dsa, W, ecfg, W.WORKLOAD_SEEDS[name], dev, 0)
+            esteps = max(3, args.steps // 4)
+            ems, etot, erec, eclk = time_steps(dsa, torch, dist, erun[-1], erun[3], dev, esteps,
+                                               3, 1, local)
+            eroof, ekern = roofline(ecfg, erec, name, esteps)
+            extra[name] = {"value": ecfg.total_q * esteps / (etot / 1e3), "unit": "tokens/s",
+                           "steps": esteps, "warmup": 3, "ms_per_step": etot / esteps,
+                           "step_ms_median": statistics.median(ems), "workload": describe(ecfg),
+                           "dtype": ecfg.kv_dtype if ecfg.idx_dtype != "e4m3" else "e4m3+bf16",
+                           "roofline": eroof, "kernels": ekern, "clocks": eclk,
+                           "gpu_launches": len(erec)}
+            del erun
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {
@@ -462,12 +397,142 @@ def main():
                        "l2": "flushed (256 MB write) before every timed step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,
-            "clocks": clk.summary(), "e2e": e2e, "gpu_launches": len(tr.records),
+            "clocks": clocks, "e2e": e2e, "gpu_launches": len(records),
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+            "workloads": extra or None,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def setup(dsa, W, cfg, seed, dev, page_size):
+    """Inputs of one workload on the device and a step that runs the DSA layer over them."""
+    import torch
+    case = W.make_case(cfg, seed)
+    d = {k: v.to(dev) for k, v in case.tensors().items()}
+    paging = {}
+    if page_size:
+        pk = W.paged_keys(case, page_size, seed)
+        d.update({k: v.to(dev) for k, v in pk.tensors().items()})
+        paging = dict(block_table=d["block_table"], page_size=page_size, num_pages=pk.num_pages)
+    P = dsa.Problem.from_config(cfg, d["cu_q"], d["cu_k"], **paging)
+    ws = dsa.Workspace(dev, P.workspace_size(5))
+    out = torch.empty(cfg.total_q, cfg.h, cfg.d_c, dtype=torch.bfloat16 if cfg.out_dtype == "bf16"
+                      else torch.float32, device=dev)
+    lse = torch.empty(cfg.total_q, cfg.h, dtype=torch.float32, device=dev)
+    idx = torch.empty(cfg.total_q, cfg.top_k, dtype=torch.int32, device=dev)
+
+    def step():
+        dsa.fused_forward(P, d["q_idx"], d["k_idx"], d["w"], d["q"], d["kv"], d.get("q_scale"),
+                          d.get("k_scale"), out=out, lse=lse, idx=idx, ws=ws)
+
+    return case, d, P, ws, out, lse, idx, step
+
+
+def time_steps(dsa, torch, dist, step, ws, dev, steps, warmup, world, local):
+    """Warm-up, then `steps` timed steps (CUDA events, L2 flushed before each, clocks sampled),
+    then the same steps again with an event pair around every launch of the library."""
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    ws.clear_status()
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    flags = ws.status()
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    # timed steps: no per-kernel events in the stream, so each kernel may start while the
+    # one before it finishes (programmatic dependent launch)
+    with ClockSampler(local) as clk:
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record()
+            step()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    # a second pass of the same steps with CUDA events around every launch (on its stream):
+    # per-kernel durations for the roofline and the launch count
+    with dsa.trace(capacity=512 * steps) as tr:  # row-chunked prefill: ~260 launches a step
+        for i in range(steps):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    return step_ms, float(t_max.item()), tr.records, clk.summary()
+
+
+def roofline(cfg, records, workload, steps):
+    """The dominant kernel against its bound (bytes for decode-shaped problems and Top-K,
+    tensor flops otherwise), and every kernel's share, mean time and achieved rate.  A stage
+    that runs in several launches a step (row chunks) is measured by its time per step."""
+    per_kernel = {}
+    for name, ms in records:
+        per_kernel.setdefault(name, []).append(ms)
+    model = work_model(cfg)
+    peaks, peak_src = load_peaks()
+    dom = max(per_kernel, key=lambda k: sum(per_kernel[k]))
+    dom_ms = sum(per_kernel[dom]) / steps
+    stage = KERNEL_STAGE.get(dom, dom)
+    decode_like = max(cfg.q_lens) == 1
+    if decode_like or stage == "topk":
+        alg = model[stage]["bytes"] if stage in model else cfg.total_q * cfg.top_k * 4
+        achieved = alg / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(dom, workload),
+                "kernel": dom, "algorithmic_bytes_per_launch": alg,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        alg = model[stage]["flops"]
+        achieved = alg / (dom_ms / 1e3) / 1e12
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                "frac": achieved / pk, "traffic": measured_traffic(dom, workload), "kernel": dom,
+                "algorithmic_flops_per_launch": alg, "peak_source": f"{peak_src} bf16_tflops"}
+    roof["kernel_ms_per_step"] = dom_ms
+    roof["launches_per_step"] = len(per_kernel[dom]) / steps
+    total = sum(sum(x) for x in per_kernel.values())
+    kernels = {k: {"launches": len(v), "ms_mean": statistics.mean(v), "share": sum(v) / total}
+               for k, v in per_kernel.items()}
+    # every kernel against its own bound (a chunked stage's launches share its work)
+    for k, v in kernels.items():
+        st = KERNEL_STAGE.get(k)
+        if st not in model:
+            continue
+        ms = sum(per_kernel[k]) / steps  # this kernel's time per step
+        if decode_like or st == "topk":
+            ach = model[st]["bytes"] / (ms / 1e3) / 1e9
+            v.update(achieved=ach, unit="GB/s", frac=ach / peaks["hbm_gbs"], ms_per_step=ms)
+        else:
+            ach = model[st]["flops"] / (ms / 1e3) / 1e12
+            v.update(achieved=ach, unit="TFLOP/s", frac=ach / peaks["bf16_tflops"],
+                     ms_per_step=ms)
+    return roof, kernels
+
+
+def one_core_baseline(workload):
+    """The oracle arm of this workload with one BLAS thread, in a child process (the thread
+    count of a BLAS library is fixed when it loads): tokens/s, or None if it failed."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        p = subprocess.run([sys.executable, os.path.abspath(__file__), "--impl", "reference",
+                            "--workload", workload, "--steps", "2", "--warmup", "1",
+                            "--ref-rows", "4"], capture_output=True, text=True, env=env,
+                           timeout=600)
+        return json.loads(p.stdout.strip().splitlines()[-1])["value"]
+    except Exception:  # a missing number is reported as such
+        return None
 
 
 if __name__ == "__main__":

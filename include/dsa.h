@@ -23,13 +23,18 @@
  *   stream).  Calls only enqueue work; argument checks are synchronous and a
  *   failing check launches nothing.
  * Workspace.  Every call takes a caller-owned device workspace of at least
- *   dsa_workspace_size() bytes.  Its first 256 bytes hold a device status word:
- *   kernels OR DSA_FLAG_* bits into it when they detect bad data (an index out
- *   of range, inconsistent cu_q/cu_k) or give up a bounded wait.  The word is
- *   sticky: clear it with dsa_clear_status() and read it with
- *   dsa_read_status().  The rest is scratch owned by the call while it runs;
- *   calls sharing one workspace must be stream-ordered.  Its contents between
- *   calls are the caller's (a call never relies on earlier contents).
+ *   dsa_workspace_size() bytes.  Its first 16384 bytes are the status block.  Its
+ *   first word is the device status word: kernels OR DSA_FLAG_* bits into it when
+ *   they detect bad data (an index out of range, inconsistent cu_q/cu_k) or give
+ *   up a bounded wait.  The word is sticky: clear it with dsa_clear_status() and
+ *   read it with dsa_read_status().  The block's other words are counters through
+ *   which the thread blocks of one kernel wait for each other; they must be zero
+ *   before the workspace's first call (a zero-filled workspace, or
+ *   dsa_clear_status()); the kernels keep them consistent from then on, also
+ *   after a call that gave up a wait.  The rest of the
+ *   workspace is scratch owned by the call while it runs; calls sharing one
+ *   workspace must be stream-ordered.  Its contents between calls are the
+ *   caller's (a call never relies on earlier contents).
  * Sequences.  Query rows and key rows are packed: sequence b owns query rows
  *   cu_q[b] .. cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1, with
  *   T_b = cu_q[b+1]-cu_q[b] <= L_b = cu_k[b+1]-cu_k[b].  The queries of a
@@ -51,7 +56,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 /* Return codes. */
 enum dsa_status {
@@ -126,7 +131,7 @@ typedef struct dsa_problem {
  * of 16}, 1 <= top_k <= 2048, max_k_len <= 2^30.  Outside them a call returns
  * DSA_ERR_UNSUPPORTED. */
 
-/* Bytes of workspace `op` needs for problem `p` (always >= 256). */
+/* Bytes of workspace `op` needs for problem `p` (always >= 16384). */
 int dsa_workspace_size(const dsa_problem* p, int op, size_t* bytes);
 
 /*
@@ -214,7 +219,7 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
  * latency-critical loops where cudaMalloc/cudaFree would synchronise the
  * device.  Such callers pass inputs and outputs but no workspace.
  *
- * Scratch is a static device array inside the library: a 256-byte status block
+ * Scratch is a static device array inside the library: a 16384-byte status block
  * plus room for 4,194,304 fp32 scores (16 MiB), held by every device that loads
  * the library until the process exits.  Problems with total_q * max_k_len above
  * 4,194,304 are rejected with DSA_ERR_UNSUPPORTED.  The call allocates nothing

@@ -18,7 +18,7 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 from . import _abi
-from ._abi import DsaError, lib  # noqa: F401
+from ._abi import STATUS_BYTES, DsaError, lib  # noqa: F401
 
 __all__ = ["Problem", "Workspace", "indexer_scores", "topk", "fused_indexer", "sparse_mla_attn",
            "fused_forward", "DsaError", "lib", "trace"]
@@ -114,17 +114,18 @@ class Problem:
 
 
 class Workspace:
-    """Caller-owned device scratch with the status word in its first 256 bytes."""
+    """Caller-owned device scratch; its first 16384 bytes are the status block (the status
+    word and the kernels' synchronisation counters, zero between calls)."""
 
-    def __init__(self, device=None, nbytes: int = 256):
+    def __init__(self, device=None, nbytes: int = STATUS_BYTES):
         self.device = torch.device(device or "cuda")
-        self.buf = torch.zeros(max(256, nbytes), dtype=torch.uint8, device=self.device)
+        self.buf = torch.zeros(max(STATUS_BYTES, nbytes), dtype=torch.uint8, device=self.device)
 
     def ensure(self, nbytes: int) -> "Workspace":
         if self.buf.numel() < nbytes:
-            flags = self.buf[:256].clone()
+            flags = self.buf[:STATUS_BYTES].clone()
             self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
-            self.buf[:256].copy_(flags)
+            self.buf[:STATUS_BYTES].copy_(flags)
         return self
 
     @property

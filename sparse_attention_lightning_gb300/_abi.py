@@ -33,7 +33,8 @@ class DsaProblem(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("block_table", ctypes.c_void_p)]
 
 
-ABI_VERSION = 2  # DSA_ABI_VERSION this binding is written for
+ABI_VERSION = 3  # DSA_ABI_VERSION this binding is written for
+STATUS_BYTES = 16384  # the workspace status block
 
 
 class DsaError(RuntimeError):

@@ -217,7 +217,8 @@ IndexerArgs indexer_args(const dsa_problem* p, const void* q_idx, const void* k_
 }
 
 // Rows that carry their own history (decode) run the one-kernel fused indexer, which keeps
-// every score on chip and needs no scratch.  Prefill-shaped problems (several queries per
+// every score on chip; its scratch holds per-row histograms and candidate lists only.
+// Prefill-shaped problems (several queries per
 // sequence: the tensor-core indexer scores blocks of four rows against each key tile) and
 // shapes that kernel does not cover score the rows in chunks: a chunk's scores go to a
 // bounded workspace buffer (sized for L2, not for the whole problem) and its Top-K reads
@@ -246,10 +247,12 @@ int chunk_rows(const dsa_problem* p) {
   return (int)(r < (size_t)p->total_q ? r : (size_t)p->total_q);
 }
 
-// Fused indexer scratch (chunked path only): a chunk's scores [rows][scores_ld] f32,
+// Fused indexer scratch: the one-kernel path's exchange buffers; for the chunked path a
+// chunk's scores [rows][scores_ld] f32,
 // histograms [rows][kHistBins] and Top-K candidate positions [rows][spill_ld]; then the
 // fused forward's indices and the attention scratch.
 struct IndexerScratch {
+  void* fused;  // the fused decode kernel's exchange buffers
   float* scores;
   uint32_t* hist;
   int32_t* spill;
@@ -267,6 +270,8 @@ size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   Carve c;
   const size_t rows = (size_t)chunk_rows(p);
   const bool tc = tc_scores(p);
+  const IndexerArgs ia = indexer_args(p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  const size_t o_fused = c.take(row_fused(p) ? indexer_topk_scratch(ia, nullptr).bytes : 0);
   const size_t o_scores = c.take(rows * scores_ld(p) * 4);
   const size_t o_hist = c.take(tc ? rows * kHistBins * 4 : 0);
   const size_t o_spill = c.take(tc ? rows * spill_ld(p) * 4 : 0);
@@ -274,6 +279,7 @@ size_t carve_indexer(const dsa_problem* p, void* ws, IndexerScratch* out) {
   const size_t o_sfa = c.take(sfa_scratch_bytes(p));
   if (out) {
     char* b = static_cast<char*>(ws);
+    out->fused = b + o_fused;
     out->scores = reinterpret_cast<float*>(b + o_scores);
     out->hist = tc ? reinterpret_cast<uint32_t*>(b + o_hist) : nullptr;
     out->spill = reinterpret_cast<int32_t*>(b + o_spill);
@@ -327,9 +333,9 @@ int run_fused_indexer(const dsa_problem* p, const void* q_idx, const void* k_idx
                       const float* q_scale, const float* k_scale, int32_t* idx, float* vals,
                       void* ws, cudaStream_t s) {
   IndexerArgs ia = indexer_args(p, q_idx, k_idx, w, q_scale, k_scale, ws);
-  if (row_fused(p)) return launch_indexer_topk(ia, p->top_k, idx, vals, s);
   IndexerScratch sc;
   carve_indexer(p, ws, &sc);
+  if (row_fused(p)) return launch_indexer_topk(ia, p->top_k, idx, vals, sc.fused, s);
   const int64_t ld = scores_ld(p);
   const bool tc = tc_scores(p);
   const int rows = chunk_rows(p);

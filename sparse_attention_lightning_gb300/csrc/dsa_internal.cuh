@@ -14,8 +14,12 @@
 namespace dsa {
 
 // ----------------------------------------------------------------------------
-// Workspace layout: [0, 256) status block; scratch regions follow, 256-aligned.
-constexpr size_t kStatusBytes = 256;
+// Workspace layout: [0, 16384) status block (word 0: status flags; word kLaunchWord: the
+// fused decode indexer's launch count; from word kRowSyncWord: its per-row counters, two
+// sets of 128 rows x 8 words); scratch regions follow, 256-aligned.
+constexpr size_t kStatusBytes = 16384;
+constexpr int kLaunchWord = 32;
+constexpr int kRowSyncWord = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -180,11 +184,21 @@ int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStrea
 bool indexer_tc_blocks4(const IndexerArgs& a);
 
 // The fused indexer for rows that carry their own history (decode): scores, head weights
-// and the causal Top-K in one kernel, one thread-block cluster per row, scores kept in
-// tensor memory; writes idx (ascending positions, -1 padded) and optionally vals.
+// and the causal Top-K in one cooperative kernel, one CTA per SM over equal shares of all
+// rows' key tiles, scores kept in tensor memory; writes idx (ascending positions, -1
+// padded) and optionally vals.  Its exchange buffers (per-row histograms and candidate
+// lists) live in `scratch` (indexer_topk_scratch(a, nullptr).bytes); the thread blocks
+// sharing a row wait for each other through the row's counter in the status block.
+struct IndexerTopkScratch {
+  size_t bytes;
+  uint32_t* hist;
+  uint32_t* rec;
+  uint2* cand;
+};
+IndexerTopkScratch indexer_topk_scratch(const IndexerArgs& a, void* base);
 bool indexer_topk_eligible(const IndexerArgs& a);
 int launch_indexer_topk(const IndexerArgs& a, int top_k, int32_t* idx, float* vals,
-                        cudaStream_t stream);
+                        void* scratch, cudaStream_t stream);
 
 // Fill scores[t, s] = -inf for pos(t) < s < ld.
 int launch_mask_tail(const Seqs& seqs, float* scores, int64_t ld, uint32_t* status,

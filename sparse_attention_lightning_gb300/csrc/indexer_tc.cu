@@ -109,14 +109,14 @@ __device__ __forceinline__ uint32_t scan_block(uint32_t v, uint32_t* ws, uint32_
     if (lane >= o) x += y;
   }
   if (lane == 31) ws[warp] = x;
-  __syncthreads();
+  cta_sync();
   uint32_t before = 0, tot = 0;
   for (int w = 0; w < NW; ++w) {
     if (w < warp) before += ws[w];
     tot += ws[w];
   }
   *total = tot;
-  __syncthreads();
+  cta_sync();
   return before + x - v;
 }
 
@@ -187,7 +187,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     cq[B] = __ldg(p.seqs.cu_q + B);
     ck[B] = __ldg(p.seqs.cu_k + B);
   }
-  __syncthreads();
+  cta_sync();
   SeqTab tabs{st, cq, ck, B};
   tabs.r0 = p.r0;
   tabs.r1 = p.r1;
@@ -214,7 +214,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
   if (warp == 1) { tmem_alloc(tmem_slot, C::TMEM_COLS); tmem_relinquish(); }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) griddep_launch();  // the Top-K kernel may be scheduled (it waits)
@@ -444,7 +444,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);

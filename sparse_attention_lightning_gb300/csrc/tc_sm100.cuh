@@ -337,10 +337,19 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// Every thread of every CTA in the cluster arrives, then waits.
+// Every thread of every CTA in the cluster arrives, then waits.  The barrier instructions
+// are warp-aligned, so the warp is reconverged first: a warp whose lanes reached the barrier
+// apart (one lane still in a role loop) would otherwise be counted at two barrier instances.
 __device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
+}
+
+// __syncthreads with the warp reconverged first (see cluster_sync).
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.

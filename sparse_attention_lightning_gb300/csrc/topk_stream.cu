@@ -53,7 +53,7 @@ __device__ __forceinline__ uint32_t scan_pair(uint32_t v, uint32_t* warp_a, uint
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_a[warp] = x;
-  __syncthreads();
+  cta_sync();
   if (warp == 0) {
     const uint32_t v0 = lane < kW ? warp_a[lane] : 0u;
     uint32_t s = v0;
@@ -65,10 +65,10 @@ __device__ __forceinline__ uint32_t scan_pair(uint32_t v, uint32_t* warp_a, uint
     __syncwarp();
     if (lane < kW) warp_a[lane] = s;
   }
-  __syncthreads();
+  cta_sync();
   const uint32_t before = (warp ? warp_a[warp - 1] : 0u) + x - v;
   *total = warp_a[kW - 1];
-  __syncthreads();
+  cta_sync();
   return before;
 }
 
@@ -82,7 +82,7 @@ __device__ __forceinline__ uint64_t scan_pair64(uint64_t v, uint64_t* warp_s, ui
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_s[warp] = x;
-  __syncthreads();
+  cta_sync();
   if (warp == 0) {
     const uint64_t v0 = lane < kW ? warp_s[lane] : 0ull;
     uint64_t z = v0;
@@ -94,10 +94,10 @@ __device__ __forceinline__ uint64_t scan_pair64(uint64_t v, uint64_t* warp_s, ui
     __syncwarp();
     if (lane < kW) warp_s[lane] = z;
   }
-  __syncthreads();
+  cta_sync();
   const uint64_t before = (warp ? warp_s[warp - 1] : 0ull) + x - v;
   *total = warp_s[kW - 1];
-  __syncthreads();
+  cta_sync();
   return before;
 }
 
@@ -111,7 +111,7 @@ __device__ __forceinline__ uint32_t suffix_above(uint32_t mine, uint32_t* warp_b
     if (lane + o < 32) x += y;
   }
   if (lane == 0) warp_b[warp] = x;
-  __syncthreads();
+  cta_sync();
   if (warp == 0) {
     const uint32_t v = lane < kW ? warp_b[lane] : 0u;
     uint32_t z = v;
@@ -123,9 +123,9 @@ __device__ __forceinline__ uint32_t suffix_above(uint32_t mine, uint32_t* warp_b
     __syncwarp();
     if (lane < kW) warp_b[lane] = z - v;
   }
-  __syncthreads();
+  cta_sync();
   const uint32_t r = warp_b[warp] + x - mine;
-  __syncthreads();
+  cta_sync();
   return r;
 }
 
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
         run += c[i];
       }
     }
-    __syncthreads();
+    cta_sync();
   }
   const uint32_t bstar = S.s_bin, above = S.s_above, nc = S.s_cnt;
   const bool in_smem = nc <= (uint32_t)kCap;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
     fetch(0);
     if (ntile > 1) fetch(1);
   }
-  __syncthreads();
+  cta_sync();
   uint32_t def_base = 0, cand_base = 0;
   int landed = 0;  // tiles consumed
   for (int ti = 0; ti < ntile; ++ti) {
@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
     // the same outcome in every thread, so that no thread is left at a barrier
     const bool ok = mbar_wait(&S.tbar[ti & 1], (ti >> 1) & 1, &abort_word, a.status,
                               DSA_FLAG_TIMEOUT);
+    __syncwarp();  // the lanes left their waits apart; the barrier below is warp-aligned
     if (__syncthreads_or(!ok)) break;
     landed = ti + 1;
     const float* tl = S.tile[ti & 1] + kKPT * tid;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
     }
     def_base += tot & 0xffffu;
     cand_base += tot >> 16;
-    __syncthreads();  // everyone is done with this buffer
+    cta_sync();  // everyone is done with this buffer
     if (tid == 0 && ti + 2 < ntile) fetch(ti + 2);
   }
   if (landed < ntile) {
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
   }
   if (tid == 0 && (def_base != above || cand_base != nc)) atomicOr(a.status, DSA_FLAG_BAD_SEQS);
   if (!in_smem) __threadfence_block();
-  __syncthreads();
+  cta_sync();
 
   // ---- exact radix select among the candidates on the low 20 bits (11 + 9); thread tid
   // takes the candidates [tid * cpt, (tid + 1) * cpt) ----
@@ -291,12 +292,12 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
     const uint32_t pmask = pass == 0 ? 0xfff00000u : 0xfffffe00u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) S.hist[8 * tid + i] = 0u;
-    __syncthreads();
+    cta_sync();
     for (uint32_t c = c_lo; c < c_hi; ++c) {
       const uint32_t kk = cand(c).x;
       if ((kk & pmask) == prefix) atomicAdd(&S.hist[(kk >> shift) & dmask], 1u);
     }
-    __syncthreads();
+    cta_sync();
     // digit (descending) where the need-th key falls: thread tid owns bins 8 tid .. 8 tid + 7
     uint32_t h[8], mine = 0;
 #pragma unroll
@@ -309,10 +310,10 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
         run += h[i];
       }
     }
-    __syncthreads();
+    cta_sync();
     need -= S.s_cnt;
     prefix |= S.s_digit << shift;
-    __syncthreads();
+    cta_sync();
   }
   const uint32_t T = prefix;  // exact key of the n-th largest; `need` of the ties are kept
 

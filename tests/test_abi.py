@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
     assert names == set(_abi.EXPORTS), names ^ set(_abi.EXPORTS)
     for n in names:
         assert hasattr(L, n), n
-    assert L.dsa_abi_version() == _abi.ABI_VERSION == 2
+    assert L.dsa_abi_version() == _abi.ABI_VERSION == 3
 
 
 def _problem(**kw):
@@ -54,7 +54,7 @@ def test_workspace_sizes(L):
     p = _problem()
     for op in (1, 2, 3, 4, 5):
         rc, n = _ws_size(L, p, op)
-        assert rc == 0 and n >= 256 and n % 256 == 0
+        assert rc == 0 and n >= _abi.STATUS_BYTES and n % 256 == 0
     assert _ws_size(L, p, 99)[0] == _abi.DSA_ERR_INVALID_ARG
 
 
