@@ -30,8 +30,9 @@
  *   read it with dsa_read_status().  The block's other words are counters through
  *   which the thread blocks of one kernel wait for each other; they must be zero
  *   before the workspace's first call (a zero-filled workspace, or
- *   dsa_clear_status()); the kernels keep them consistent from then on, also
- *   after a call that gave up a wait.  The rest of the
+ *   dsa_clear_status()), and every call that completes without DSA_FLAG_TIMEOUT
+ *   leaves them consistent.  After a call that set DSA_FLAG_TIMEOUT, call
+ *   dsa_clear_status() before the next one.  The rest of the
  *   workspace is scratch owned by the call while it runs; calls sharing one
  *   workspace must be stream-ordered.  Its contents between calls are the
  *   caller's (a call never relies on earlier contents).

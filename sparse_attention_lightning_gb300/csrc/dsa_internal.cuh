@@ -16,10 +16,15 @@ namespace dsa {
 // ----------------------------------------------------------------------------
 // Workspace layout: [0, 16384) status block (word 0: status flags; word kLaunchWord: the
 // fused decode indexer's launch count; from word kRowSyncWord: its per-row counters, two
-// sets of 128 rows x 8 words); scratch regions follow, 256-aligned.
+// sets of 128 rows x 8 words; from word kPieceWord: the sparse attention's piece counts);
+// scratch regions follow, 256-aligned.
 constexpr size_t kStatusBytes = 16384;
 constexpr int kLaunchWord = 32;
 constexpr int kRowSyncWord = 256;
+// from word kPieceWord: the sparse attention's per-(row, CTA half) counts of the pieces of
+// a cut row whose partials are written (reset by the piece that merges them)
+constexpr int kPieceWord = kRowSyncWord + 2 * 128 * 8;
+constexpr int kPieceRows = (int)(kStatusBytes / 4 - kPieceWord) / 2;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

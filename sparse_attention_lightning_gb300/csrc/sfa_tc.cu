@@ -48,9 +48,11 @@
 // Work schedule.  With many query rows, cluster c takes whole rows c, c + clusters, ...
 // With few (decode), the rows' chunk slots (ceil(top_k / 64) per row) are laid end to
 // end and cut into one contiguous, equal share per cluster, so every cluster gathers
-// the same number of chunks; a row cut by share boundaries is attended in pieces, each
-// piece writes its partial (O, max, sum), and a second kernel (sfa_combine_kernel, all
-// SMs) merges each cut row's pieces in piece order.
+// the same number of chunks; a row cut by share boundaries is attended in pieces.  Each
+// piece but the row's first writes its partial (O, max, sum) and counts itself in; the
+// first piece, the last one its cluster attends (the others come first in theirs), waits
+// for the others' count, then merges their partials with its own O, still in tensor
+// memory, in piece order.
 // Every wait is bounded (DSA_FLAG_TIMEOUT).
 #include <cuda_fp16.h>
 
@@ -104,6 +106,7 @@ struct Params {
   float4* part_o;    // [(total_q + clusters - 1) * 2][64][128] float4 (pieces)
   float* part_ml;    // [(total_q + clusters - 1) * 2][128][2]
   int32_t* lists;    // [gridDim.x][kMaxTopK]: each CTA's compacted cache rows of its unit
+  uint32_t* pcount;  // [total_q][2]: pieces of a cut row whose partials are written, by CTA half
   uint32_t* status;
 };
 
@@ -255,7 +258,6 @@ sfa_tc_kernel(Params p) {
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (p.pieces && threadIdx.x == 0) griddep_launch();  // the merge kernel may be scheduled (it waits)
 
   if (warp == 0 || warp == 10) {
     // -------- producer warps: index compaction (warp 0), gathers (32 rows each) --------
@@ -739,8 +741,8 @@ sfa_tc_kernel(Params p) {
         if (rank == 0 && half == 0 && p.lse)
           p.lse[(int64_t)t * kH + h] =
               ltot > 0.f ? (m_ref + log2f(ltot)) * 0.69314718055994531f : -INFINITY;
-      } else {
-        // a piece of a cut row: its partial (O, m, l), merged by sfa_combine_kernel
+      } else if (cluster_id != cf) {
+        // a piece of a cut row (not its first): its partial (O, m, l), then it counts itself in
         const int64_t slot = (int64_t)(cluster_id + t) * 2 + rank;
         float4* po = p.part_o + slot * (64 * kH);
         for (int b = 0; b < 4; ++b) {
@@ -759,6 +761,93 @@ sfa_tc_kernel(Params p) {
           p.part_ml[(slot * kH + h) * 2] = m_ref;
           p.part_ml[(slot * kH + h) * 2 + 1] = ltot;
         }
+        __syncwarp();
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps' writes are done
+        if (warp == 2 && lane == 0) {
+          __threadfence();
+          atomicAdd(p.pcount + 2 * t + rank, 1u);
+        }
+      } else {
+        // the row's first piece: once the others have counted themselves in, out =
+        // Σ_j w_j O_j / Σ_j w_j l_j with w_j = 2^(m_j - M), M = max m_j over the pieces with
+        // keys, summed in piece order (this piece, the first, from tensor memory)
+        if (warp == 2 && lane == 0) {
+          uint32_t* pc = p.pcount + 2 * t + rank;
+          const uint64_t t0 = globaltimer_ns();
+          while (*reinterpret_cast<volatile uint32_t*>(pc) < (uint32_t)(np - 1)) {
+            if (*abort_flag) break;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(p.status, DSA_FLAG_TIMEOUT);
+              break;
+            }
+            __nanosleep(32);
+          }
+          __threadfence();
+          *pc = 0u;  // every other piece has counted itself in: reset for the next call
+        }
+        __syncwarp();
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+        float M = ltot > 0.f ? m_ref : -INFINITY;
+        for (int j = 1; j < np; ++j) {
+          const float2 v = __ldcg(ml + ((int64_t)(cf + j + t) * 2 + rank) * kH + h);
+          if (v.y > 0.f) M = fmaxf(M, v.x);
+        }
+        const float wl = ltot > 0.f ? ex2(m_ref - M) : 0.f;
+        float wsum = wl * ltot;
+        for (int j = 1; j < np; ++j) {
+          const float2 v = __ldcg(ml + ((int64_t)(cf + j + t) * 2 + rank) * kH + h);
+          if (v.y > 0.f) wsum = fmaf(ex2(v.x - M), v.y, wsum);
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        uint8_t* orow = static_cast<uint8_t*>(p.out) +
+                        (((int64_t)t * kH + h) * kDC + gbase + ocol) * (p.out_f32 ? 4 : 2);
+        for (int b = 0; b < 4; ++b) {  // 32 of the thread's 128 columns at a time
+          uint32_t r[32];
+          if (have) tmem_ld32(lane_base + kOCol + ocol + 32 * b, r);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = wl * __uint_as_float(r[i]);
+          for (int j = 1; j < np; ++j) {
+            const int64_t sl = (int64_t)(cf + j + t) * 2 + rank;
+            const float2 v = __ldcg(ml + sl * kH + h);
+            const float w = v.y > 0.f ? ex2(v.x - M) : 0.f;
+            const float4* src = p.part_o + sl * (64 * kH) + (32 * half + 8 * b) * kH + h;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = __ldcg(src + i * kH);
+              acc[4 * i] = fmaf(w, x.x, acc[4 * i]);
+              acc[4 * i + 1] = fmaf(w, x.y, acc[4 * i + 1]);
+              acc[4 * i + 2] = fmaf(w, x.z, acc[4 * i + 2]);
+              acc[4 * i + 3] = fmaf(w, x.w, acc[4 * i + 3]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] *= inv;
+          if (p.out_f32) {
+            float4* op = reinterpret_cast<float4*>(orow) + 8 * b;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) op[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+          } else {
+            uint4* op = reinterpret_cast<uint4*>(orow) + 4 * b;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * i + 2 * e], acc[8 * i + 2 * e + 1]);
+                w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              op[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+        if (rank == 0 && half == 0 && p.lse)
+          p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -771,74 +860,6 @@ sfa_tc_kernel(Params p) {
   }
 }
 
-// Merge of the cut rows' pieces.  Thread = (query row t, CTA half `rank`, head h, group
-// of 8 column quads R = 8g .. 8g + 7, i.e. output columns gbase + 32g .. + 31); lanes run
-// along h, so every partial read is a coalesced 512-byte line, and a thread has 8 (or
-// 16) reads in flight.  With piece j's (O_j, m_j, l_j), M = max m_j over the pieces with
-// keys and w_j = 2^(m_j - M):  out = Σ_j w_j O_j / Σ_j w_j l_j, summed in piece order
-// (the same arithmetic whichever order the pieces finished in).
-__global__ void __launch_bounds__(256) sfa_combine_kernel(Params p) {
-  griddep_wait();  // the pieces' partials are complete
-  const int t = blockIdx.x >> 3;
-  const int rank = (blockIdx.x >> 2) & 1;
-  const int g = ((blockIdx.x & 3) << 1) | (threadIdx.x >> 7);
-  const int h = threadIdx.x & 127;
-  int cf, np;
-  row_pieces(p, t, p.nclusters, cf, np);
-  if (np == 1) return;
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int j = 0; j < np; ++j) {
-    const float2 v = __ldg(ml + ((int64_t)(cf + j + t) * 2 + rank) * kH + h);
-    if (v.y > 0.f) M = fmaxf(M, v.x);
-  }
-  float wsum = 0.f;
-  float4 acc[8];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int j = 0; j < np; ++j) {
-    const int64_t sl = (int64_t)(cf + j + t) * 2 + rank;
-    const float2 v = __ldg(ml + sl * kH + h);
-    const float4* src = p.part_o + sl * (64 * kH) + (8 * g) * kH + h;
-    float4 x[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) x[r] = __ldg(src + r * kH);
-    const float w = v.y > 0.f ? ex2(v.x - M) : 0.f;
-    wsum = fmaf(w, v.y, wsum);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      acc[r].x = fmaf(w, x[r].x, acc[r].x);
-      acc[r].y = fmaf(w, x[r].y, acc[r].y);
-      acc[r].z = fmaf(w, x[r].z, acc[r].z);
-      acc[r].w = fmaf(w, x[r].w, acc[r].w);
-    }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int64_t o = ((int64_t)t * kH + h) * kDC + (rank ? 256 : 0) + 32 * g;
-  if (p.out_f32) {
-    float4* op = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      op[r] = make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
-  } else {
-    uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 a = acc[2 * i], b = acc[2 * i + 1];
-      const __nv_bfloat162 w0 = __floats2bfloat162_rn(a.x * inv, a.y * inv);
-      const __nv_bfloat162 w1 = __floats2bfloat162_rn(a.z * inv, a.w * inv);
-      const __nv_bfloat162 w2 = __floats2bfloat162_rn(b.x * inv, b.y * inv);
-      const __nv_bfloat162 w3 = __floats2bfloat162_rn(b.z * inv, b.w * inv);
-      op[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&w0), *reinterpret_cast<const uint32_t*>(&w1),
-                         *reinterpret_cast<const uint32_t*>(&w2), *reinterpret_cast<const uint32_t*>(&w3));
-    }
-  }
-  if (rank == 0 && g == 0 && p.lse)
-    p.lse[(int64_t)t * kH + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
-}
-
 }  // namespace
 
 bool sfa_tc_eligible(const SfaArgs& a) {
@@ -848,8 +869,11 @@ bool sfa_tc_eligible(const SfaArgs& a) {
 }
 
 // Equal contiguous shares of the rows' chunk slots (pieces) when whole rows would load
-// the clusters unevenly: fewer than four rows per cluster.
-bool sfa_tc_pieces(int total_q) { return total_q > 0 && total_q < 2 * num_sms(); }
+// the clusters unevenly: fewer than four rows per cluster (and no more rows than the
+// status block has piece counts for).
+bool sfa_tc_pieces(int total_q) {
+  return total_q > 0 && total_q < 2 * num_sms() && total_q <= kPieceRows;
+}
 
 // Per-CTA compacted key-row lists (the grid has at most num_sms CTAs), then, with pieces,
 // the partial (O, m, l) slots: one per cluster and row it touches, slot = cluster + row <
@@ -878,6 +902,7 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   p.out = a.out;
   p.lse = a.lse;
   p.status = a.status;
+  p.pcount = a.status + kPieceWord;
   char* b = static_cast<char*>(scratch);
   p.lists = reinterpret_cast<int32_t*>(b);
   b += align_up((size_t)num_sms() * kMaxTopK * 4, 256);
@@ -902,13 +927,7 @@ int launch_sfa_tc(const SfaArgs& a, void* scratch, cudaStream_t stream) {
   DSA_LAUNCH("sfa_tc", stream,
              e = launch_pdl(kern, dim3(2 * clusters), dim3(kThreads), kSmem, stream, p));
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_tc: %s", cudaGetErrorString(e));
-  int rc = check_launch("sfa_tc");
-  if (rc != DSA_OK || !pieces) return rc;
-  DSA_LAUNCH("sfa_combine", stream,
-             e = launch_pdl(sfa_combine_kernel, dim3((unsigned)a.seqs.total_q * 8), dim3(256), 0,
-                            stream, p));
-  if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "sfa_combine: %s", cudaGetErrorString(e));
-  return check_launch("sfa_combine");
+  return check_launch("sfa_tc");
 }
 
 }  // namespace dsa
