@@ -37,9 +37,18 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # summarised under profiles/, valid only for the kernel sources it was taken with: a change to
 # any of them (their hash differs) makes the figure unknown again.
 MEASURED_TRAFFIC = {
-    # (kernel, workload): (bytes per launch, sources, sha256 prefix of the sources)
-    ("sfa_tc", "decode"): (82_842_880, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                           "f78bf02fbf027691"),
+    # (kernel, workload): (bytes per launch, sources, sha256 prefix of the sources); a kernel
+    # whose sources changed since the capture reports null (profiles/ has the captures)
+    ("indexer_topk_bf16", "decode"): (179_345_664, ("indexer_topk.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "4347068d89e8dea2"),
+    ("sfa_tc", "decode"): (83_910_400, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "203efdfbc5fe2ea1"),
+    ("sfa_tc", "prefill_8k"): (2_322_682_624, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "203efdfbc5fe2ea1"),
+    ("topk_stream", "prefill_8k"): (33_485_056, ("topk_stream.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "2b1df69854b37618"),
+    ("indexer_tc_bf16_qb4", "prefill_8k"): (58_224_640, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "c4b82c62c6fd0a83"),
 }
 
 
