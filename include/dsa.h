@@ -236,8 +236,16 @@ int dsa_fused_indexer_static(const dsa_problem* p, const void* q_idx, const void
                              const float* w, const float* q_scale, const float* k_scale,
                              int32_t* idx, float* vals, uint32_t* flags_out, void* stream);
 
-/* Zero the workspace status word (enqueued on `stream`). */
+/* Zero the workspace status block (the status word and the kernels' counters; enqueued on
+ * `stream`). */
 int dsa_clear_status(void* ws, void* stream);
+
+/* Self-test of the bounded-wait path every kernel's waits go through: one thread waits on an
+ * mbarrier that nothing arrives at, gives up after limit_ns (0 < limit_ns <= 1e8) and ORs
+ * DSA_FLAG_TIMEOUT into the status word of `ws` (enqueued on `stream`; no other effect: the
+ * context stays usable).  DSA_ERR_WORKSPACE for a NULL or misaligned `ws`,
+ * DSA_ERR_INVALID_ARG for a limit out of range. */
+int dsa_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
 
 /* Synchronise `stream`, then copy the workspace status word into *flags.
  * Returns DSA_ERR_TIMEOUT if DSA_FLAG_TIMEOUT is set, DSA_OK otherwise. */

@@ -139,6 +139,11 @@ class Workspace:
     def clear_status(self) -> None:
         _abi.check(lib().dsa_clear_status(self.ptr, _stream(self.device)))
 
+    def selftest_wait_timeout(self, limit_ns: int = 1_000_000) -> None:
+        """Run the bounded-wait self-test: a wait on an mbarrier nothing arrives at gives up
+        after limit_ns and sets DSA_FLAG_TIMEOUT in this workspace's status word."""
+        _abi.check(lib().dsa_selftest_wait_timeout(self.ptr, int(limit_ns), _stream(self.device)))
+
     def status(self) -> int:
         """Synchronise the current stream and return the device status flags."""
         f = ctypes.c_uint32(0)

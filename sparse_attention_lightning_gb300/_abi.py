@@ -17,7 +17,8 @@ OP_INDEXER_SCORES, OP_TOPK, OP_FUSED_INDEXER, OP_SPARSE_MLA_ATTN, OP_FUSED_FORWA
 EXPORTS = ("dsa_workspace_size", "dsa_indexer_scores", "dsa_topk", "dsa_fused_indexer",
            "dsa_sparse_mla_attn", "dsa_fused_forward", "dsa_clear_status", "dsa_read_status",
            "dsa_status_str", "dsa_last_error", "dsa_abi_version", "dsa_trace_begin",
-           "dsa_trace_end", "dsa_trace_count", "dsa_trace_get", "dsa_fused_indexer_static")
+           "dsa_trace_end", "dsa_trace_count", "dsa_trace_get", "dsa_fused_indexer_static",
+           "dsa_selftest_wait_timeout")
 
 
 class DsaProblem(ctypes.Structure):
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
         "dsa_fused_forward": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "dsa_fused_indexer_static": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "dsa_clear_status": [vp, vp],
+        "dsa_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
         "dsa_read_status": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
         "dsa_abi_version": [],
         "dsa_trace_begin": [ctypes.c_int],

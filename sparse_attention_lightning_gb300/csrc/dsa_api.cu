@@ -10,8 +10,21 @@
 #include <vector>
 
 #include "dsa_internal.cuh"
+#include "tc_sm100.cuh"
 
 namespace dsa {
+
+// One thread waits, through the kernels' bounded wait, on an mbarrier that nothing arrives at:
+// it gives up after limit_ns, ORs DSA_FLAG_TIMEOUT into the status word and returns.
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  tc::mbar_init(&bar, 1);
+  abort_flag = 0;
+  tc::fence_barrier_init();
+  tc::mbar_wait_for(&bar, 0, limit_ns, &abort_flag, status, DSA_FLAG_TIMEOUT);
+}
 
 // ----------------------------------------------------------------------------
 // Errors.
@@ -515,6 +528,17 @@ int dsa_read_status(const void* ws, void* stream, uint32_t* flags) {
   if (e != cudaSuccess) return set_error(DSA_ERR_CUDA, "read_status: %s", cudaGetErrorString(e));
   if (*flags & DSA_FLAG_TIMEOUT) return set_error(DSA_ERR_TIMEOUT, "device wait timed out");
   return DSA_OK;
+}
+
+int dsa_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream) {
+  if (!ws) return set_error(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned16(ws)) return set_error(DSA_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+  if (limit_ns == 0 || limit_ns > 100000000ull)
+    return set_error(DSA_ERR_INVALID_ARG, "limit_ns must be in (0, 1e8]");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DSA_LAUNCH("wait_selftest", s,
+             wait_selftest_kernel<<<1, 32, 0, s>>>(static_cast<uint32_t*>(ws), limit_ns));
+  return check_launch("wait_selftest");
 }
 
 int dsa_trace_begin(int capacity) {

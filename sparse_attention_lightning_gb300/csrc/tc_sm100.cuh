@@ -80,10 +80,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
 }
 
 // Wait until the phase of `bar` with parity `parity` has completed.  Gives up
-// (returns false) when *abort is set by another thread or after kWaitLimitNs;
-// a give-up by timeout sets *abort and ORs `flag` into *status.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, uint32_t flag) {
+// (returns false) when *abort is set by another thread or after limit_ns; a give-up by
+// timeout sets *abort and ORs `flag` into *status.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort, uint32_t* status, uint32_t flag) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -91,13 +91,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(addr, parity)) return true;
     if ((i & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(status, flag);
         return false;
       }
     }
   }
+}
+// The kernels' waits: limit kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status, uint32_t flag) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs, abort, status, flag);
 }
 
 // Time-bounded wait that ignores the abort flag: used when draining copies or
