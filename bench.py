@@ -392,6 +392,10 @@ def main():
                            "gpu_launches": len(erec)}
             del erun
             torch.cuda.empty_cache()
+            if ecfg.idx_dtype == "e4m3":
+                extra[name]["topk_recall_vs_bf16"] = fp8_recall(dsa, W, ecfg,
+                                                                W.WORKLOAD_SEEDS[name], dev)
+                torch.cuda.empty_cache()
 
     if rank == 0:
         line = {
@@ -413,6 +417,38 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def topk_recall(a, b):
+    """Per-row recall of Top-K rows ``a`` against ``b`` (int32 [rows, k], -1 padded):
+    |a ∩ b| / |b| over each row's valid entries (device tensors)."""
+    import torch
+    rows, k = b.shape
+    big = 1 << 32
+    base = torch.arange(rows, device=b.device, dtype=torch.int64)[:, None] * big
+    va, vb = a >= 0, b >= 0
+    hit = torch.isin((a.long() + base)[va], (b.long() + base)[vb])
+    per = torch.zeros(rows, device=b.device, dtype=torch.float64)
+    per.index_add_(0, torch.nonzero(va)[:, 0], hit.double())
+    return per / vb.sum(1).clamp(min=1).double()
+
+
+def fp8_recall(dsa, W, cfg, seed, dev, nseq=16):
+    """Top-K recall of the FP8 indexer against the bf16 indexer on the bf16 values it was
+    quantised from (the same seeded streams), over the workload's first nseq sequences."""
+    import dataclasses
+    sub = W.first_sequences(cfg, nseq)
+    res = {}
+    for dt in ("e4m3", "bf16"):
+        c = dataclasses.replace(sub, idx_dtype=dt)
+        case = W.make_case(c, seed, attention=False)
+        d = {k: v.to(dev) for k, v in case.tensors().items() if v.numel()}
+        P = dsa.Problem.from_config(c, d["cu_q"], d["cu_k"])
+        res[dt], _ = dsa.fused_indexer(P, d["q_idx"], d["k_idx"], d["w"], d.get("q_scale"),
+                                       d.get("k_scale"))
+    r = topk_recall(res["e4m3"], res["bf16"])
+    return {"mean": float(r.mean()), "min": float(r.min()), "rows": int(r.numel()),
+            "sample": f"the workload's first {nseq} sequences ({sub.total_k} keys)"}
 
 
 def setup(dsa, W, cfg, seed, dev, page_size):

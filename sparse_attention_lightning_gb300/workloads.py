@@ -136,8 +136,10 @@ def decode_lengths(batch: int, lo: int, hi: int, seed: int) -> List[int]:
     return [int(v) for v in torch.randint(lo, hi + 1, (batch,), generator=g)]
 
 
-def make_case(cfg: Config, seed: int) -> Case:
-    """Draw every input of ``cfg`` from streams seeded by ``seed``."""
+def make_case(cfg: Config, seed: int, attention: bool = True) -> Case:
+    """Draw every input of ``cfg`` from streams seeded by ``seed`` (``attention=False``: the
+    indexer's inputs only, q and kv left empty).  A config holding the first sequences of
+    another draws exactly that config's first rows (every stream is drawn in row order)."""
     B = cfg.num_seqs
     for t, l in zip(cfg.q_lens, cfg.k_lens):
         if t > l:
@@ -163,8 +165,12 @@ def make_case(cfg: Config, seed: int) -> Case:
         q_idx = _normal((TQ, cfg.h_idx, cfg.d_idx), sd_i, _gen(seed, "q_idx"), idd)
         k_idx = _normal((TK, cfg.d_idx), sd_i, _gen(seed, "k_idx"), idd)
     w = torch.rand(TQ, cfg.h_idx, generator=_gen(seed, "w"), dtype=torch.float32)
-    q = _normal((TQ, cfg.h, cfg.d), sd_m, _gen(seed, "q"), kvd)
-    kv = _normal((TK, cfg.d), sd_m, _gen(seed, "kv"), kvd)
+    if attention:
+        q = _normal((TQ, cfg.h, cfg.d), sd_m, _gen(seed, "q"), kvd)
+        kv = _normal((TK, cfg.d), sd_m, _gen(seed, "kv"), kvd)
+    else:
+        q = torch.empty(0, dtype=kvd)
+        kv = torch.empty(0, dtype=kvd)
     return Case(cfg, cu_q, cu_k, q_idx, k_idx, w, q, kv, q_scale, k_scale)
 
 
@@ -275,3 +281,9 @@ def paged_keys(case: Case, page_size: int, seed: int, spare_pages: int = 3) -> P
     k_scale = scatter(case.k_scale, 1.0e4) if case.k_scale is not None else None
     return PagedKeys(page_size, num_pages, table, scatter(case.k_idx, fill_idx),
                      scatter(case.kv, 100.0), k_scale)
+
+
+def first_sequences(cfg: Config, n: int) -> Config:
+    """The config of ``cfg``'s first ``n`` sequences (same dims)."""
+    return dataclasses.replace(cfg, name=f"{cfg.name}_first{n}", q_lens=list(cfg.q_lens[:n]),
+                               k_lens=list(cfg.k_lens[:n]))
