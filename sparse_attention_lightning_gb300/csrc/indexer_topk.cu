@@ -70,6 +70,10 @@ constexpr int kSub = 32;                 // candidates bucketed by key bits 20..
 constexpr int kNB2 = 128, kNB3 = 512;    // later rounds: key bits 15..9, 8..0
 constexpr int kRec = kSub + 4;           // a run's record: bucket counts, keys above B*, pad
 constexpr int kRowWords = 8;             // a row counter's own 32 bytes
+// In the split of the tiles, every row's tiles are preceded by this many placeholder tiles,
+// so a CTA whose share crosses a row start (and then selects for two runs, ~6 µs more)
+// streams that many fewer tiles (~0.7 µs each) and ends with the others.
+constexpr int kRowLead = 8;
 // A row's counter (status block) has three 8-bit fields: the row's histogram is clear (set
 // by the CTA holding its first tile), and the CTAs holding runs of the row whose counts,
 // and whose candidates, are in.  There are two sets: a launch uses set (epoch & 1) and
@@ -156,6 +160,7 @@ struct Params {
 
 struct Xch {
   uint32_t epoch;                  // this launch's number
+  uint32_t mytiles;                // the CTA's tiles
   uint32_t res[4];                 // find_digit's answer
   uint32_t gtb, eqb;               // kept keys above / equal to T before the run
   uint32_t ncand;                  // the run's candidates staged
@@ -366,8 +371,10 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     skip = rk == rn && p.vals == nullptr;  // every key kept and no score wanted
     my_nt = skip ? 0 : (rn + kBM - 1) / kBM;
   }
+  // positions in the split: the rows' tiles in order, each row's after kRowLead placeholders
+  const int lead = my_nt > 0 ? kRowLead : 0;
   uint32_t tall;
-  const int start = (int)block_scan((uint32_t)my_nt, scan_ws, &tall);
+  const int start = (int)block_scan((uint32_t)(lead + my_nt), scan_ws, &tall) + lead;
   for (int c = tid; c <= G; c += kThreads) tb[c] = (int)((int64_t)c * tall / G);
   cta_sync();
   const int G0 = tb[g], G1 = tb[g + 1];
@@ -396,8 +403,8 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     Run& r = runs[ri_];
     r.t = tid; r.b = ri.b; r.n = rn; r.k = rk; r.k0 = ri.k0;
     r.start = start; r.nt = my_nt;
-    r.l0 = max(start, G0) - G0;
-    r.l1 = min(start + my_nt, G1) - G0;
+    r.l0 = 0;  // the CTA's tiles are numbered after the placeholders are left out (below)
+    r.l1 = min(start + my_nt, G1) - max(start, G0);
     r.j0 = max(start, G0) - start;
     r.pgo = r.pg0 = 0;
     r.nr = nr;
@@ -410,10 +417,20 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     r.bstar = r.above = 0u;
   }
   if (owned) own[oi] = make_int2(tid, rn);
-  const int mytiles = G1 - G0;
-  const int npairs = (mytiles + kPair - 1) / kPair;
-  if (tid == 0) X->epoch = ticket / (uint32_t)G;
   cta_sync();
+  if (tid == 0) {
+    X->epoch = ticket / (uint32_t)G;
+    int acc = 0;  // the runs' tiles, numbered consecutively
+    for (int i = 0; i < ns; ++i) {
+      runs[i].l0 = acc;
+      acc += runs[i].l1;
+      runs[i].l1 = acc;
+    }
+    X->mytiles = acc;
+  }
+  cta_sync();
+  const int mytiles = (int)X->mytiles;
+  const int npairs = (mytiles + kPair - 1) / kPair;
   const uint32_t epoch = X->epoch;
   uint32_t* rsync = p.rowsync + (epoch & 1u) * (kMaxRows * kRowWords);  // this launch's set
   if (tid == 0) {
@@ -1207,7 +1224,7 @@ bool indexer_topk_eligible(const IndexerArgs& a) {
   const int64_t ntiles = ((int64_t)a.seqs.max_k_len + kBM - 1) / kBM;
   return (a.idx_dtype == DSA_BF16 || a.idx_dtype == DSA_FP8_E4M3) && a.h_idx == kHI &&
          a.d_idx == kDI && a.seqs.total_q <= kMaxRows &&
-         (int64_t)a.seqs.total_q * ntiles <= (int64_t)num_sms() * kMaxTiles &&
+         (int64_t)a.seqs.total_q * (ntiles + kRowLead) <= (int64_t)num_sms() * kMaxTiles &&
          (a.idx_dtype != DSA_FP8_E4M3 || (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0);
 }
 
