@@ -138,8 +138,6 @@ int check_ptr(const void* p, const char* name, bool nullable = false) {
   return DSA_OK;
 }
 
-size_t dtype_size(int dt) { return dt == DSA_F32 ? 4 : dt == DSA_BF16 ? 2 : 1; }
-
 int check_problem(const dsa_problem* p, bool need_indexer, bool need_attn) {
   if (!p) return set_error(DSA_ERR_INVALID_ARG, "problem descriptor is NULL");
   if (p->num_seqs < 1) return set_error(DSA_ERR_INVALID_ARG, "num_seqs = %d", p->num_seqs);

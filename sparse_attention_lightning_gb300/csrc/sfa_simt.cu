@@ -162,13 +162,6 @@ int launch_typed(const SfaArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t sfa_simt_smem_bytes(int d_c, int d_rope, int top_k) {
-  const int D = d_c + d_rope;
-  return sizeof(float) * ((size_t)kMaxHeads * D + (size_t)kChunk * (D + 1) +
-                          (size_t)kMaxHeads * d_c + kMaxHeads * kChunk + 3 * kMaxHeads) +
-         sizeof(int) * (size_t)top_k;
-}
-
 int launch_sfa_simt(const SfaArgs& a, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
   if (a.kv_dtype == DSA_F32 && a.out_dtype == DSA_F32) return launch_typed<float, float>(a, stream);

@@ -858,6 +858,15 @@ sfa_tc_kernel(Params p) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // On the normal path every peer copy into this CTA completed on an x_full phase that a wait
+  // above consumed, and every remote arrive precedes the peer's release at the cluster
+  // barrier.  After a timeout a consumer may have stopped waiting while a 4 KB copy the peer
+  // issued before its own barrier arrival is still landing: such a CTA stays resident for a
+  // further 100 us (far longer than a shared-memory copy takes) before it exits.
+  if (threadIdx.x == 0 && *abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) __nanosleep(1000);
+  }
 }
 
 }  // namespace
