@@ -115,7 +115,7 @@ KERNEL_STAGE = {
     "indexer_tc_bf16_qb4": "indexer", "indexer_tc_fp8_qb4": "indexer",
     "indexer_topk_bf16": "indexer", "indexer_topk_fp8": "indexer",
     "topk_rows": "topk", "topk_smem": "topk", "topk_stream": "topk",
-    "sfa_simt": "sfa", "sfa_tc": "sfa", "sfa_combine": "sfa_merge",
+    "sfa_simt": "sfa", "sfa_tc": "sfa",
 }
 
 
@@ -396,6 +396,12 @@ def main():
                 extra[name]["topk_recall_vs_bf16"] = fp8_recall(dsa, W, ecfg,
                                                                 W.WORKLOAD_SEEDS[name], dev)
                 torch.cuda.empty_cache()
+        # the indexer prolog (Q quantisation + head-weight projection, one launch) on the
+        # query batches of the two decode workloads
+        extra["indexer_prolog"] = {
+            name: prolog_record(dsa, W, torch, dist, dev, local, W.workload(name),
+                                W.WORKLOAD_SEEDS[name], max(3, args.steps // 4))
+            for name in ("decode", "fp8_decode")}
 
     if rank == 0:
         line = {
@@ -449,6 +455,37 @@ def fp8_recall(dsa, W, cfg, seed, dev, nseq=16):
     r = topk_recall(res["e4m3"], res["bf16"])
     return {"mean": float(r.mean()), "min": float(r.min()), "rows": int(r.numel()),
             "sample": f"the workload's first {nseq} sequences ({sub.total_k} keys)"}
+
+
+def prolog_record(dsa, W, torch, dist, dev, local, cfg, seed, steps):
+    """The indexer prolog on ``cfg``'s query tokens: timed like a step (L2 flushed before
+    each), against HBM with its algorithmic bytes (bf16 q_proj, x and W_h read once; E4M3
+    codes, per-head scales and fp32 weights written once)."""
+    inp = {k: v.to(dev) for k, v in W.prolog_inputs(cfg, seed).items()}
+    T, h, d = inp["q_proj"].shape
+    dm = inp["x"].shape[1]
+    codes = torch.empty(T, h, d, dtype=torch.uint8, device=dev)
+    scale = torch.empty(T, h, dtype=torch.float32, device=dev)
+    w = torch.empty(T, h, dtype=torch.float32, device=dev)
+    ws = dsa.Workspace(dev)
+
+    def step():
+        dsa.indexer_prolog(inp["q_proj"], inp["x"], inp["w_h"], codes, scale, w)
+
+    ms, tot, rec, clk = time_steps(dsa, torch, dist, step, ws, dev, steps, 3, 1, local)
+    alg = T * h * d * 2 + T * h * d + 2 * T * h * 4 + T * dm * 2 + h * dm * 2
+    kms = statistics.mean(m for _, m in rec)
+    peaks, src = load_peaks()
+    ach = alg / (kms / 1e3) / 1e9
+    return {"value": T * steps / (tot / 1e3), "unit": "tokens/s", "steps": steps, "warmup": 3,
+            "ms_per_step": tot / steps, "step_ms_median": statistics.median(ms),
+            "workload": f"indexer prolog: T={T} tokens, H_I={h}, d_I={d}, d_model={dm}, bf16 in, "
+                        f"E4M3 codes + per-token scale + fp32 head weights out",
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "indexer_prolog", "algorithmic_bytes_per_launch": alg,
+                         "kernel_ms": kms, "peak_source": f"{src} hbm_gbs"},
+            "clocks": clk, "gpu_launches": len(rec)}
 
 
 def setup(dsa, W, cfg, seed, dev, page_size):

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 
 /* Return codes. */
 enum dsa_status {
@@ -235,6 +235,34 @@ int dsa_fused_forward(const dsa_problem* p, const void* q_idx, const void* k_idx
 int dsa_fused_indexer_static(const dsa_problem* p, const void* q_idx, const void* k_idx,
                              const float* w, const float* q_scale, const float* k_scale,
                              int32_t* idx, float* vals, uint32_t* flags_out, void* stream);
+
+/*
+ * The indexer prolog: Q quantisation and the head-weight projection, the two
+ * input-preparation steps that share one stream ahead of the fused indexer
+ * ("… New-Architecture LLMs" §4.2 Three-Stream Coordination for Indexer
+ * Preprocessing: q_quant = quant(q_proj), w_proj = W_h @ x; "Optimizing LLM
+ * Inference for New Architectures", §3), fused into one launch.  For token t:
+ *   amax = max |q_proj[t, :, :]|,  scale = amax / 448 (fp32; 1 if amax = 0)
+ *   q_codes[t, j, e] = E4M3(q_proj[t, j, e] / scale)  (fp32 division, round to
+ *                      nearest even, saturated to ±448)
+ *   q_scale[t, j]    = scale for every head j (one scale per token)
+ *   w[t, j]          = Σ_c W_h[j, c] · x[t, c]   (fp32 accumulation)
+ * These are the FP8 inputs (q_idx, q_scale, w) of dsa_fused_indexer.
+ * q_proj  [total_q, h_idx, d_idx] bf16, d_idx a multiple of 8, or NULL (no
+ *         quantisation; q_codes and q_scale are then ignored);
+ * x       [total_q, d_model] bf16 and w_h [h_idx, d_model] bf16, d_model a
+ *         positive multiple of 8, or both NULL (no projection; w ignored);
+ * q_codes [total_q, h_idx, d_idx] uint8 (E4M3 codes), q_scale [total_q, h_idx]
+ *         f32, w [total_q, h_idx] f32: outputs, caller-owned device memory.
+ * q_proj, x, w_h and q_codes are 16-byte aligned; q_scale and w 4-byte.
+ * One launch on `stream`, no workspace.  total_q = 0 launches nothing and
+ * accepts NULL pointers.
+ * DSA_ERR_INVALID_ARG for missing or misaligned pointers (or all inputs NULL),
+ * DSA_ERR_UNSUPPORTED for sizes outside those limits.
+ */
+int dsa_indexer_prolog(int32_t total_q, int32_t h_idx, int32_t d_idx, int32_t d_model,
+                       const void* q_proj, const void* x, const void* w_h, uint8_t* q_codes,
+                       float* q_scale, float* w, void* stream);
 
 /* Zero the workspace status block (the status word and the kernels' counters; enqueued on
  * `stream`). */

@@ -21,7 +21,7 @@ from . import _abi
 from ._abi import STATUS_BYTES, DsaError, lib  # noqa: F401
 
 __all__ = ["Problem", "Workspace", "indexer_scores", "topk", "fused_indexer", "sparse_mla_attn",
-           "fused_forward", "DsaError", "lib", "trace"]
+           "fused_forward", "indexer_prolog", "DsaError", "lib", "trace"]
 
 _DT = {torch.float32: _abi.DSA_F32, torch.bfloat16: _abi.DSA_BF16,
        torch.uint8: _abi.DSA_FP8_E4M3, torch.float8_e4m3fn: _abi.DSA_FP8_E4M3}
@@ -246,6 +246,48 @@ def fused_indexer(P: Problem, q_idx, k_idx, w, q_scale=None, k_scale=None, idx=N
         ctypes.byref(P.c), q_idx.data_ptr(), k_idx.data_ptr(), w.data_ptr(), _ptr(q_scale),
         _ptr(k_scale), idx.data_ptr(), _ptr(vals), ws.ptr, ws.nbytes, _stream(dev)))
     return idx, vals
+
+
+def indexer_prolog(q_proj=None, x=None, w_h=None, q_codes=None, q_scale=None, w=None):
+    """Q quantisation and head-weight projection in one launch (dsa_indexer_prolog).
+
+    q_proj [T, H_I, d_I] bf16 -> (q_codes [T, H_I, d_I] uint8 E4M3, q_scale [T, H_I] f32);
+    x [T, d_model] bf16, w_h [H_I, d_model] bf16 -> w [T, H_I] f32.  Either part may be
+    left out (None inputs).  Returns (q_codes, q_scale, w), None for a part not computed.
+    """
+    if q_proj is None and x is None:
+        raise ValueError("indexer_prolog needs q_proj or (x, w_h)")
+    if q_proj is not None:
+        T, h, d = q_proj.shape
+    else:
+        T, h = x.shape[0], w_h.shape[0]
+        d = 8
+    dev = (q_proj if q_proj is not None else x).device
+    d_model = 0
+    if q_proj is not None:
+        _need(q_proj, "q_proj", _abi.DSA_BF16, (T, h, d))
+        if q_codes is None:
+            q_codes = torch.empty((T, h, d), dtype=torch.uint8, device=dev)
+        if q_scale is None:
+            q_scale = torch.empty((T, h), dtype=torch.float32, device=dev)
+        _need(q_codes, "q_codes", _abi.DSA_FP8_E4M3, (T, h, d))
+        _need(q_scale, "q_scale", _abi.DSA_F32, (T, h))
+    else:
+        q_codes = q_scale = None
+    if x is not None or w_h is not None:
+        if x is None or w_h is None:
+            raise ValueError("x and w_h go together")
+        d_model = x.shape[1]
+        _need(x, "x", _abi.DSA_BF16, (T, d_model))
+        _need(w_h, "w_h", _abi.DSA_BF16, (h, d_model))
+        if w is None:
+            w = torch.empty((T, h), dtype=torch.float32, device=dev)
+        _need(w, "w", _abi.DSA_F32, (T, h))
+    else:
+        w = None
+    _abi.check(lib().dsa_indexer_prolog(T, h, d, d_model, _ptr(q_proj), _ptr(x), _ptr(w_h),
+                                        _ptr(q_codes), _ptr(q_scale), _ptr(w), _stream(dev)))
+    return q_codes, q_scale, w
 
 
 def _attn_out(P: Problem, out, lse, device, want_lse: bool):

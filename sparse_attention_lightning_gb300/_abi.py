@@ -18,7 +18,7 @@ EXPORTS = ("dsa_workspace_size", "dsa_indexer_scores", "dsa_topk", "dsa_fused_in
            "dsa_sparse_mla_attn", "dsa_fused_forward", "dsa_clear_status", "dsa_read_status",
            "dsa_status_str", "dsa_last_error", "dsa_abi_version", "dsa_trace_begin",
            "dsa_trace_end", "dsa_trace_count", "dsa_trace_get", "dsa_fused_indexer_static",
-           "dsa_selftest_wait_timeout")
+           "dsa_selftest_wait_timeout", "dsa_indexer_prolog")
 
 
 class DsaProblem(ctypes.Structure):
@@ -34,7 +34,7 @@ class DsaProblem(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("block_table", ctypes.c_void_p)]
 
 
-ABI_VERSION = 3  # DSA_ABI_VERSION this binding is written for
+ABI_VERSION = 4  # DSA_ABI_VERSION this binding is written for
 STATUS_BYTES = 16384  # the workspace status block
 
 
@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
         "dsa_fused_indexer_static": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "dsa_clear_status": [vp, vp],
         "dsa_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
+        "dsa_indexer_prolog": [ctypes.c_int32] * 4 + [vp] * 7,
         "dsa_read_status": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
         "dsa_abi_version": [],
         "dsa_trace_begin": [ctypes.c_int],

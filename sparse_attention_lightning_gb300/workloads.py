@@ -17,7 +17,12 @@ bf16 8k prefill, bf16 64k prefill, FP8-indexer decode):
 * decode context lengths integer-uniform (inclusive) in the stated range;
 * FP8 indexer inputs: bf16-valued data quantised per token (one fp32 scale
   per key row, one per query token broadcast over its heads), scale =
-  amax/448, codes = E4M3 round-to-nearest-even of x/scale.
+  amax/448, codes = E4M3 round-to-nearest-even of x/scale;
+* indexer prolog inputs (``prolog_inputs``): the bf16 indexer query before
+  quantisation (the same draw the FP8 query codes are made from), a hidden
+  state ``x[ΣT, d_model]`` ~ N(0, 1) and a head-weight projection
+  ``W_h[H_I, d_model]`` ~ N(0, 1/d_model), both bf16.  The pages give no
+  hidden width; 7168 is used for the DSA workloads.
 
 All tensors live on the host (torch CPU); callers move them to the device.
 """
@@ -33,7 +38,7 @@ F32, BF16, FP8 = "f32", "bf16", "e4m3"
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Stable ids so each tensor gets its own stream for a given seed.
-_STREAM_IDS = {"lens": 1, "q_idx": 2, "k_idx": 3, "w": 4, "q": 5, "kv": 6}
+_STREAM_IDS = {"lens": 1, "q_idx": 2, "k_idx": 3, "w": 4, "q": 5, "kv": 6, "x": 7, "w_h": 8}
 
 _CHUNK = 1 << 24  # values drawn per generator call (bounds host temporaries)
 
@@ -287,3 +292,19 @@ def first_sequences(cfg: Config, n: int) -> Config:
     """The config of ``cfg``'s first ``n`` sequences (same dims)."""
     return dataclasses.replace(cfg, name=f"{cfg.name}_first{n}", q_lens=list(cfg.q_lens[:n]),
                                k_lens=list(cfg.k_lens[:n]))
+
+
+D_MODEL = 7168  # hidden width of the prolog's head-weight projection (not given by the pages)
+
+
+def prolog_inputs(cfg: Config, seed: int, d_model: int = D_MODEL) -> Dict[str, torch.Tensor]:
+    """The indexer prolog's inputs for ``cfg``'s query tokens: ``q_proj`` [ΣT, H_I, d_I] bf16
+    (drawn from the stream the FP8 query codes are quantised from, so quantising it gives
+    exactly ``make_case(cfg).q_idx`` of an FP8 config), ``x`` [ΣT, d_model] bf16 and ``w_h``
+    [H_I, d_model] bf16."""
+    TQ = cfg.total_q
+    q_proj = _normal((TQ, cfg.h_idx * cfg.d_idx), cfg.d_idx ** -0.5, _gen(seed, "q_idx"),
+                     torch.bfloat16).view(TQ, cfg.h_idx, cfg.d_idx)
+    x = _normal((TQ, d_model), 1.0, _gen(seed, "x"), torch.bfloat16)
+    w_h = _normal((cfg.h_idx, d_model), d_model ** -0.5, _gen(seed, "w_h"), torch.bfloat16)
+    return {"q_proj": q_proj, "x": x, "w_h": w_h}

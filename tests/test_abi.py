@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(L):
     assert names == set(_abi.EXPORTS), names ^ set(_abi.EXPORTS)
     for n in names:
         assert hasattr(L, n), n
-    assert L.dsa_abi_version() == _abi.ABI_VERSION == 3
+    assert L.dsa_abi_version() == _abi.ABI_VERSION == 4
 
 
 def _problem(**kw):

@@ -123,3 +123,120 @@ def test_head_weights_ones_give_row_sums():
     x = rng.integers(-4, 5, size=(4, 20)).astype(np.float64)
     w = P.head_weights(x, np.ones((3, 20)))
     assert np.array_equal(w, np.repeat(x.sum(axis=1)[:, None], 3, axis=1))
+
+
+# ---------------------------------------------------------------------------
+# The library: argument checks (no GPU work) and, on the GPU, parity.
+
+def test_prolog_argument_checks():
+    from sparse_attention_lightning_gb300 import _abi
+    L = _abi.lib()
+    a = 1 << 20  # an aligned address that is never dereferenced: every check fails first
+    assert L.dsa_indexer_prolog(4, 4, 32, 64, None, None, None, None, None, None, None) == \
+        _abi.DSA_ERR_INVALID_ARG
+    assert L.dsa_indexer_prolog(4, 4, 12, 64, a, None, None, a, a, None, None) == \
+        _abi.DSA_ERR_UNSUPPORTED
+    assert L.dsa_indexer_prolog(4, 4, 32, 60, None, a, a, None, None, a, None) == \
+        _abi.DSA_ERR_UNSUPPORTED
+    assert L.dsa_indexer_prolog(4, 4, 32, 64, None, a, None, None, None, a, None) == \
+        _abi.DSA_ERR_INVALID_ARG
+    assert L.dsa_indexer_prolog(4, 4, 32, 64, a + 8, None, None, a, a, None, None) == \
+        _abi.DSA_ERR_INVALID_ARG
+    assert L.dsa_indexer_prolog(-1, 4, 32, 64, a, None, None, a, a, None, None) == \
+        _abi.DSA_ERR_INVALID_ARG
+
+
+def _w_bound(x: np.ndarray, w_h: np.ndarray) -> np.ndarray:
+    # fp32 accumulation of exact bf16 products: each output is rounded at most
+    # (d_model/2048 + 8 + 5 + 8) times along its summation tree, each time by at
+    # most 2^-24 of a partial sum bounded by Σ|terms|; 1e-5 covers d_model <= 16384
+    return 1e-5 * (np.abs(x) @ np.abs(w_h).T) + 1e-30
+
+
+def _run_prolog(T, h, d, d_model, seed, parts=("q", "w")):
+    import sparse_attention_lightning_gb300 as dsa
+    from sparse_attention_lightning_gb300 import workloads as W
+    cfg = W.custom([1] * T, [64] * T, h_idx=h, d_idx=d, idx_dtype="e4m3", kv_dtype="bf16")
+    inp = W.prolog_inputs(cfg, seed, d_model)
+    dev = "cuda:0"
+    qp = inp["q_proj"].to(dev) if "q" in parts else None
+    x = inp["x"].to(dev) if "w" in parts else None
+    wh = inp["w_h"].to(dev) if "w" in parts else None
+    codes, scale, w = dsa.indexer_prolog(qp, x, wh)
+    torch.cuda.synchronize()
+    return inp, codes, scale, w
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,h,d,d_model", [
+    (3, 4, 32, 64),        # one partial tile of each kind
+    (37, 64, 128, 7168),   # decode shapes: five token tiles, the last ragged
+    (32, 64, 128, 7168),   # the 32-sequence decode batch
+    (129, 12, 16, 200),    # ragged head tile, d_model not a multiple of the thread stride
+    (1, 1, 8, 8),          # smallest sizes
+])
+def test_prolog_matches_oracle(T, h, d, d_model):
+    inp, codes, scale, w = _run_prolog(T, h, d, d_model, seed=T + h)
+    qf = inp["q_proj"].float().reshape(T, h * d).numpy()
+    rc, rs = P.quantise_tokens(qf)
+    assert np.array_equal(codes.cpu().reshape(T, -1).numpy(), rc)      # bit-exact codes
+    assert np.array_equal(scale.cpu().numpy(), np.repeat(rs[:, None], h, axis=1))
+    x = inp["x"].float().numpy().astype(np.float64)
+    wh = inp["w_h"].float().numpy().astype(np.float64)
+    ref = P.head_weights(x, wh)
+    err = np.abs(w.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= _w_bound(x, wh)), float((err / _w_bound(x, wh)).max())
+
+
+@pytest.mark.gpu
+def test_prolog_parts_and_edge_tokens():
+    import sparse_attention_lightning_gb300 as dsa
+    dev = "cuda:0"
+    # quantisation only, with an all-zero token and a token holding one huge value
+    q = torch.randn(5, 8, 64).to(torch.bfloat16)
+    q[1] = 0
+    q[3, 2, 7] = 3.0e38
+    codes, scale, w = dsa.indexer_prolog(q.to(dev))
+    assert w is None
+    rc, rs = P.quantise_tokens(q.float().reshape(5, -1).numpy())
+    assert np.array_equal(codes.cpu().reshape(5, -1).numpy(), rc)
+    assert np.array_equal(scale.cpu().numpy()[:, 0], rs) and rs[1] == 1.0
+    # projection only
+    inp, codes, scale, w = _run_prolog(9, 16, 32, 520, seed=7, parts=("w",))
+    assert codes is None and scale is None
+    x = inp["x"].float().numpy().astype(np.float64)
+    wh = inp["w_h"].float().numpy().astype(np.float64)
+    assert np.all(np.abs(w.cpu().numpy() - P.head_weights(x, wh)) <= _w_bound(x, wh))
+    # no tokens: nothing launched, empty results
+    c0, s0, w0 = dsa.indexer_prolog(torch.empty(0, 4, 32, dtype=torch.bfloat16, device=dev))
+    assert c0.numel() == 0 and s0.numel() == 0
+
+
+@pytest.mark.gpu
+def test_prolog_feeds_the_fp8_fused_indexer():
+    """prolog -> FP8 fused indexer on the GPU against the oracle's prolog -> indexer -> Top-K:
+    the GPU prolog's query codes and scales are those of the FP8 workload's inputs, and the
+    selected positions match the oracle's under the Top-K tie rule."""
+    import dataclasses
+
+    import sparse_attention_lightning_gb300 as dsa
+    from oracle import dsa_oracle as O
+    from sparse_attention_lightning_gb300 import workloads as W
+    from tests.parity import check_topk_row
+    cfg = W.custom([1] * 5, [3000, 700, 4096, 1500, 2200], h_idx=64, d_idx=128, h=128, d_c=512,
+                   d_rope=64, top_k=512, idx_dtype="e4m3", kv_dtype="bf16")
+    case = W.make_case(cfg, seed=21)
+    inp = W.prolog_inputs(cfg, 21, 1024)
+    dev = "cuda:0"
+    codes, scale, w = dsa.indexer_prolog(inp["q_proj"].to(dev), inp["x"].to(dev),
+                                         inp["w_h"].to(dev))
+    assert torch.equal(codes.cpu(), case.q_idx) and torch.equal(scale.cpu(), case.q_scale)
+    Pb = dsa.Problem.from_config(cfg, case.cu_q.to(dev), case.cu_k.to(dev))
+    idx, _ = dsa.fused_indexer(Pb, codes, case.k_idx.to(dev), w, scale, case.k_scale.to(dev))
+    idx = idx.cpu().numpy()
+    x = inp["x"].float().numpy().astype(np.float64)
+    wh = inp["w_h"].float().numpy().astype(np.float64)
+    ref_w = P.head_weights(x, wh).astype(np.float32)
+    prob = O.problem_from_case(dataclasses.replace(case, w=torch.from_numpy(ref_w)))
+    for t in range(cfg.total_q):
+        check_topk_row(idx[t], prob.scores(t), cfg.top_k, ctx=f"row {t}")
