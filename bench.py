@@ -4,8 +4,11 @@
 
 One step = one dsa_fused_forward over one batch of the workload (all of the
 path's steps: scoring, head weighting, Top-K, gather, attention), inputs
-resident in HBM.  L2 is flushed (a 256 MB write) before every timed step,
-outside the step's CUDA events.  Prints one JSON line on rank 0.
+resident in HBM.  L2 is flushed before every timed step, outside the step's
+CUDA events: a 256 MB write, then a 256 MB read of another buffer, so that the
+lines the write left dirty are written back before the step starts (a
+write-only flush leaves L2 full of dirty lines whose write-back the step's first
+kernel would pay for).  Prints one JSON line on rank 0.
 
 Under torchrun (N > 1) every rank runs its own batch (seed offset by rank; the
 sequences are independent, so no collective is on the data path): weak scaling,
@@ -413,7 +416,7 @@ def main():
             "config": {"workload": describe(cfg) + (f" paged={args.page_size}" if args.page_size
                                                     else ""),
                        "tokens_per_step_per_gpu": cfg.total_q,
-                       "l2": "flushed (256 MB write) before every timed step",
+                       "l2": "flushed before every timed step (256 MB write, then 256 MB read)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu,
             "clocks": clocks, "e2e": e2e, "gpu_launches": len(records),
@@ -516,9 +519,16 @@ def time_steps(dsa, torch, dist, step, ws, dev, steps, warmup, world, local):
     """Warm-up, then `steps` timed steps (CUDA events, L2 flushed before each, clocks sampled),
     then the same steps again with an event pair around every launch of the library."""
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    clean = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()                    # evicts the step's data
+        torch.sum(clean, 0, out=sink)    # evicts the dirty flush lines (written back now)
+
     ws.clear_status()
     for _ in range(warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     flags = ws.status()
@@ -533,7 +543,7 @@ def time_steps(dsa, torch, dist, step, ws, dev, steps, warmup, world, local):
     # one before it finishes (programmatic dependent launch)
     with ClockSampler(local) as clk:
         for i in range(steps):
-            flush.zero_()
+            flush_l2()
             evs[i][0].record()
             step()
             evs[i][1].record()
@@ -544,7 +554,7 @@ def time_steps(dsa, torch, dist, step, ws, dev, steps, warmup, world, local):
     # per-kernel durations for the roofline and the launch count
     with dsa.trace(capacity=512 * steps) as tr:  # row-chunked prefill: ~260 launches a step
         for i in range(steps):
-            flush.zero_()
+            flush_l2()
             step()
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in evs]

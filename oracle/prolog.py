@@ -8,7 +8,8 @@ inputs ("Day0 Inference Adaptation and Performance Optimization for
 New-Architecture LLMs", §4.2 Three-Stream Coordination for Indexer
 Preprocessing: q_quant = quant(q_proj) and w_proj = W_h @ x on the third
 stream; "Optimizing LLM Inference for New Architectures", §3 Three-stream
-coordination; "Day0 … on Ascend", §2.2 Indexer Prolog):
+coordination; "Day0 Inference Optimization for New Architecture LLMs Based on
+CANN", §2.2 Indexer Prolog Three-Stream Coordination):
 
 1. Q quantisation.  The indexer query q_proj[t] (all H_I·d_I elements of token
    t) becomes FP8 E4M3 codes with one fp32 scale per token, the format the FP8

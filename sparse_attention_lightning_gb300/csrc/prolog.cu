@@ -5,15 +5,19 @@
 // projection share one stream; "Optimizing LLM Inference for New
 // Architectures", §3).
 //
-//   Q quantisation: one CTA per token.  The token's H_I·d_I query elements are
-//     read twice (the second read hits L1): first their absolute maximum, then
-//     each element divided by scale = amax / 448 and rounded to E4M3 (nearest
-//     even, saturating).  Both divisions are IEEE fp32 (__fdiv_rn), so the codes
-//     are a function of the inputs alone, not of the compiler's division.
-//   Head-weight projection: w = x · W_hᵀ, one CTA per tile of 8 tokens × 8
-//     heads.  Its threads split d_model in 16-byte chunks; each chunk of the 8
-//     W_h rows is widened once and used for all 8 tokens.  fp32 accumulation,
-//     then a warp butterfly and a sum over the 8 warps.
+//   Q quantisation: one CTA per token.  The token's H_I·d_I query elements
+//     (up to 8192) are loaded once into registers, all loads in flight together:
+//     first their absolute maximum, then each element divided by scale =
+//     amax / 448 and rounded to E4M3 (nearest even, saturating).  Both
+//     divisions are IEEE fp32 (__fdiv_rn), so the codes are a function of the
+//     inputs alone, not of the compiler's division.  Longer tokens take a
+//     two-pass loop.
+//   Head-weight projection: w = x · W_hᵀ, one CTA per tile of 4 tokens × 8
+//     heads.  Its threads split d_model in 16-byte chunks.  Each chunk's 12 row
+//     loads are issued before any is used (rows past the end are clamped to the
+//     last one and their sums dropped), so a chunk costs one memory latency,
+//     not one per row.  fp32 accumulation, then a transpose-reduce across
+//     each warp and a sum over the 16 warps.
 //
 // Both kinds of CTA run in the same grid (quantisation first), so the prolog
 // is one launch on the caller's stream.  The outputs are what the FP8 fused
@@ -26,10 +30,11 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTB = 8;  // tokens of one projection tile
-constexpr int kHB = 8;  // heads of one projection tile
+constexpr int kTB = 4;      // tokens of one projection tile
+constexpr int kHB = 8;      // heads of one projection tile
+constexpr int kQChunks = 2;  // 16-byte chunks of a token per thread kept in registers
 
 struct PrologParams {
   const uint4* q_proj;  // [T, n8] chunks of 8 bf16
@@ -52,14 +57,41 @@ __device__ __forceinline__ void widen8(const uint4& v, float (&f)[8]) {
   }
 }
 
+__device__ __forceinline__ float absmax8(const uint4& v, float m) {
+  float f[8];
+  widen8(v, f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  return m;
+}
+
+__device__ __forceinline__ uint2 codes8(const uint4& v, float scale) {
+  float f[8];
+  widen8(v, f);
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    b[i] = __nv_cvt_float_to_fp8(__fdiv_rn(f[i], scale), __NV_SATFINITE, __NV_E4M3);
+  return make_uint2(b[0] | b[1] << 8 | b[2] << 16 | b[3] << 24,
+                    b[4] | b[5] << 8 | b[6] << 16 | b[7] << 24);
+}
+
 __device__ void quantise_token(const PrologParams& p, int t, float* red) {
   const uint4* src = p.q_proj + (size_t)t * p.n8;
+  uint2* dst = p.q_codes + (size_t)t * p.n8;
+  const bool resident = p.n8 <= kThreads * kQChunks;
+  uint4 v[kQChunks];
   float m = 0.f;
-  for (int c = threadIdx.x; c < p.n8; c += kThreads) {
-    float f[8];
-    widen8(__ldg(src + c), f);
+  if (resident) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    for (int i = 0; i < kQChunks; ++i) {
+      const int c = threadIdx.x + i * kThreads;
+      v[i] = c < p.n8 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kQChunks; ++i) m = absmax8(v[i], m);
+  } else {
+    for (int c = threadIdx.x; c < p.n8; c += kThreads) m = absmax8(__ldg(src + c), m);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -70,16 +102,14 @@ __device__ void quantise_token(const PrologParams& p, int t, float* red) {
   for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[i]);
   const float scale = m > 0.f ? __fdiv_rn(m, 448.f) : 1.f;
 
-  uint2* dst = p.q_codes + (size_t)t * p.n8;
-  for (int c = threadIdx.x; c < p.n8; c += kThreads) {
-    float f[8];
-    widen8(__ldg(src + c), f);
-    uint32_t b[8];
+  if (resident) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      b[i] = __nv_cvt_float_to_fp8(__fdiv_rn(f[i], scale), __NV_SATFINITE, __NV_E4M3);
-    dst[c] = make_uint2(b[0] | b[1] << 8 | b[2] << 16 | b[3] << 24,
-                        b[4] | b[5] << 8 | b[6] << 16 | b[7] << 24);
+    for (int i = 0; i < kQChunks; ++i) {
+      const int c = threadIdx.x + i * kThreads;
+      if (c < p.n8) dst[c] = codes8(v[i], scale);
+    }
+  } else {
+    for (int c = threadIdx.x; c < p.n8; c += kThreads) dst[c] = codes8(__ldg(src + c), scale);
   }
   for (int j = threadIdx.x; j < p.h; j += kThreads) p.q_scale[(size_t)t * p.h + j] = scale;
 }
@@ -87,6 +117,13 @@ __device__ void quantise_token(const PrologParams& p, int t, float* red) {
 __device__ void project_tile(const PrologParams& p, int tile, float* red) {
   const int t0 = (tile / p.head_tiles) * kTB, j0 = (tile % p.head_tiles) * kHB;
   const int nt = min(kTB, p.T - t0), nh = min(kHB, p.h - j0);
+  // rows past the end repeat the last row: their loads stay in bounds, their sums are dropped
+  const uint4* xrow[kTB];
+  const uint4* wrow[kHB];
+#pragma unroll
+  for (int tt = 0; tt < kTB; ++tt) xrow[tt] = p.x + (size_t)(t0 + min(tt, nt - 1)) * p.dm8;
+#pragma unroll
+  for (int j = 0; j < kHB; ++j) wrow[j] = p.w_h + (size_t)(j0 + min(j, nh - 1)) * p.dm8;
   float acc[kTB][kHB];
 #pragma unroll
   for (int a = 0; a < kTB; ++a)
@@ -94,38 +131,45 @@ __device__ void project_tile(const PrologParams& p, int tile, float* red) {
     for (int b = 0; b < kHB; ++b) acc[a][b] = 0.f;
 
   for (int c = threadIdx.x; c < p.dm8; c += kThreads) {
-    float wv[kHB][8];
+    uint4 xr[kTB], wr[kHB];
+#pragma unroll
+    for (int tt = 0; tt < kTB; ++tt) xr[tt] = __ldg(xrow[tt] + c);
+#pragma unroll
+    for (int j = 0; j < kHB; ++j) wr[j] = __ldg(wrow[j] + c);
+    float xf[kTB][8];
+#pragma unroll
+    for (int tt = 0; tt < kTB; ++tt) widen8(xr[tt], xf[tt]);
 #pragma unroll
     for (int j = 0; j < kHB; ++j) {
-      if (j < nh) {
-        widen8(__ldg(p.w_h + (size_t)(j0 + j) * p.dm8 + c), wv[j]);
-      } else {
+      float wf[8];
+      widen8(wr[j], wf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) wv[j][e] = 0.f;
-      }
-    }
+      for (int tt = 0; tt < kTB; ++tt)
 #pragma unroll
-    for (int tt = 0; tt < kTB; ++tt) {
-      if (tt < nt) {
-        float xv[8];
-        widen8(__ldg(p.x + (size_t)(t0 + tt) * p.dm8 + c), xv);
-#pragma unroll
-        for (int j = 0; j < kHB; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[tt][j] = fmaf(wv[j][e], xv[e], acc[tt][j]);
-      }
+        for (int e = 0; e < 8; ++e) acc[tt][j] = fmaf(wf[e], xf[tt][e], acc[tt][j]);
     }
   }
+  // Transpose-reduce the warp's 32 sums (one per (token, head) of the tile) in 31 shuffles:
+  // at each halving step a lane keeps the half of its values its lane bit selects and adds the
+  // partner's copy of that half; afterwards lane l holds value l summed over the warp.
+  static_assert(kTB * kHB == 32, "one value per lane after the transpose-reduce");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float v[32];
 #pragma unroll
   for (int tt = 0; tt < kTB; ++tt)
 #pragma unroll
-    for (int j = 0; j < kHB; ++j) {
-      float v = acc[tt][j];
+    for (int j = 0; j < kHB; ++j) v[tt * kHB + j] = acc[tt][j];
 #pragma unroll
-      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) red[warp * kTB * kHB + tt * kHB + j] = v;
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = lane & o;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
+  }
+  red[warp * kTB * kHB + lane] = v[0];
   __syncthreads();
   if (threadIdx.x < kTB * kHB) {
     const int tt = threadIdx.x / kHB, j = threadIdx.x % kHB;

@@ -148,8 +148,9 @@ def test_prolog_argument_checks():
 
 def _w_bound(x: np.ndarray, w_h: np.ndarray) -> np.ndarray:
     # fp32 accumulation of exact bf16 products: each output is rounded at most
-    # (d_model/2048 + 8 + 5 + 8) times along its summation tree, each time by at
-    # most 2^-24 of a partial sum bounded by Σ|terms|; 1e-5 covers d_model <= 16384
+    # d_model/512 + 8 (a thread's chunks) + 5 (warp butterfly) + 16 (warps) times,
+    # each time by at most 2^-24 of a partial sum bounded by Σ|terms|; 1e-5 covers
+    # d_model <= 65536
     return 1e-5 * (np.abs(x) @ np.abs(w_h).T) + 1e-30
 
 
