@@ -15,6 +15,12 @@ layer computes:
    (ReLU and the weight form are the DSA indexer definition; the pages give the
    dot → weighted-sum order.)  FP8 inputs are dequantised exactly first:
    q_I[t, j, :] = code · q_scale[t, j], k_I[s, :] = code · k_scale[s].
+   MXFP8 inputs ("… New-Architecture LLMs" §5.1 Index Path: Fully Quantized with
+   MXFP8 Per-Group; "Optimizing LLM Inference for New Architectures", §4: one
+   scale per 32 elements) carry one E8M0 scale (2^(e − 127)) per 32 consecutive
+   elements of a query head or a key:
+   q_I[t, j, c] = code · 2^(q_scale[t, j, c/32] − 127),
+   k_I[s, c] = code · 2^(k_scale[s, c/32] − 127).
 2. Causal Top-K ("… New-Architecture LLMs" §4.1 and §6.2: index computation is
    causal, later positions see a longer history): the min(k, pos+1) positions
    with the largest I, ties broken toward the smaller position.
@@ -62,13 +68,26 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return sign * val
 
 
+def e8m0_to_f64(codes: np.ndarray) -> np.ndarray:
+    """OCP E8M0 scale (the MX formats' shared scale): 2^(code − 127); 255 is NaN."""
+    c = np.ascontiguousarray(codes).view(np.uint8).astype(np.float64)
+    return np.where(c == 255, np.nan, np.exp2(c - 127.0))
+
+
+def mx_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """E4M3 codes [..., n] with one E8M0 scale per 32 consecutive elements [..., n/32]."""
+    v = e4m3_to_f64(codes)
+    s = e8m0_to_f64(scales)
+    return v * np.repeat(s, 32, axis=-1)
+
+
 def to_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
     """Decode an array stored as 'f32' (float32), 'bf16' (uint16/int16 bits) or 'e4m3' (uint8 codes)."""
     if dtype == "f32":
         return np.asarray(arr, dtype=np.float32).astype(np.float64)
     if dtype == "bf16":
         return bf16_to_f64(arr)
-    if dtype == "e4m3":
+    if dtype in ("e4m3", "mxfp8"):
         return e4m3_to_f64(arr)
     if dtype == "f64":
         return np.asarray(arr, dtype=np.float64)
@@ -140,8 +159,9 @@ class Problem:
     """Inputs of one DSA problem, decoded to fp64 lazily per sequence / row.
 
     ``arrays`` maps names to numpy arrays as stored ('bf16' as uint16 bits,
-    'e4m3' as uint8 codes): cu_q, cu_k, q_idx, k_idx, w, q, kv and, for FP8,
-    q_scale [ΣT, H_I] and k_scale [ΣL].
+    'e4m3' and 'mxfp8' as uint8 codes): cu_q, cu_k, q_idx, k_idx, w, q, kv and, for
+    FP8, q_scale [ΣT, H_I] and k_scale [ΣL] (fp32); for MXFP8, q_scale
+    [ΣT, H_I, d_I/32] and k_scale [ΣL, d_I/32] (E8M0 bytes).
     """
 
     def __init__(self, arrays: Dict[str, np.ndarray], *, idx_dtype: str, kv_dtype: str,
@@ -163,7 +183,10 @@ class Problem:
     def k_idx_seq(self, b: int) -> np.ndarray:
         if b not in self._k_cache:
             lo, hi = self.cu_k[b], self.cu_k[b + 1]
-            k = to_f64(self.a["k_idx"][lo:hi], self.idx_dtype)
+            if self.idx_dtype == "mxfp8":
+                k = mx_dequant(self.a["k_idx"][lo:hi], self.a["k_scale"][lo:hi])
+            else:
+                k = to_f64(self.a["k_idx"][lo:hi], self.idx_dtype)
             if self.idx_dtype == "e4m3":
                 k = k * np.asarray(self.a["k_scale"][lo:hi], dtype=np.float64)[:, None]
             self._k_cache = {b: k}            # keep one sequence decoded at a time
@@ -181,6 +204,8 @@ class Problem:
         return to_f64(self.a["kv"][self.cu_k[b] + sel], self.kv_dtype)
 
     def q_idx_row(self, t: int) -> np.ndarray:
+        if self.idx_dtype == "mxfp8":
+            return mx_dequant(self.a["q_idx"][t], self.a["q_scale"][t])
         q = to_f64(self.a["q_idx"][t], self.idx_dtype)
         if self.idx_dtype == "e4m3":
             q = q * np.asarray(self.a["q_scale"][t], dtype=np.float64)[:, None]

@@ -111,6 +111,55 @@ def test_indexer_fp8_scales_dequantise_per_key_and_per_query_head():
                            p8.scores(0))
 
 
+def test_e8m0_decode_matches_torch_for_every_code():
+    # OCP E8M0: 2^(code - 127), 255 = NaN (the library's own float8_e8m0fnu)
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).double().numpy()
+    got = O.e8m0_to_f64(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[:255], ref[:255])
+    assert O.e8m0_to_f64(np.array([127, 128, 126], np.uint8)).tolist() == [1.0, 2.0, 0.5]
+
+
+def test_mxfp8_group_scales_sit_on_their_32_elements():
+    # codes all 1.0 (0x38); query groups scaled 1, 2, 4, 8 and key groups 8, 4, 2, 1: the dot
+    # is 32·(8 + 8 + 8 + 8) = 1024, while a reversed or transposed group axis gives 2720
+    HI, DI, L = 2, 128, 3
+    qc = np.full((1, HI, DI), 0x38, np.uint8)
+    kc = np.full((L, DI), 0x38, np.uint8)
+    qs = np.array([[[127, 128, 129, 130], [130, 129, 128, 127]]], np.uint8)
+    ks = np.tile(np.array([[130, 129, 128, 127]], np.uint8), (L, 1))
+    w = np.array([[1.0, 0.25]], np.float32)
+    p = O.Problem(dict(cu_q=np.array([0, 1]), cu_k=np.array([0, L]), w=w, q_idx=qc, k_idx=kc,
+                       q_scale=qs, k_scale=ks, q=np.zeros((1, 1, 8), np.float32),
+                       kv=np.zeros((L, 8), np.float32)),
+                  idx_dtype="mxfp8", kv_dtype="f32", d_c=4, top_k=2)
+    # head 0: 32·(1·8 + 2·4 + 4·2 + 8·1) = 1024; head 1: 32·(8·8 + 4·4 + 2·2 + 1·1) = 2720
+    assert p.scores(0).tolist() == [1.0 * 1024 + 0.25 * 2720] * L
+
+
+def test_indexer_mxfp8_equals_fp32_on_dequantised_values():
+    rng = np.random.default_rng(3)
+    T, L, HI, DI = 1, 7, 3, 64
+    qc = rng.integers(0, 256, (T, HI, DI)).astype(np.uint8)
+    kc = rng.integers(0, 256, (L, DI)).astype(np.uint8)
+    qc[(qc & 0x7F) == 0x7F] = 0x3C
+    kc[(kc & 0x7F) == 0x7F] = 0x3C
+    qs = rng.integers(120, 134, (T, HI, DI // 32)).astype(np.uint8)
+    ks = rng.integers(120, 134, (L, DI // 32)).astype(np.uint8)
+    w = rng.uniform(0, 1, (T, HI)).astype(np.float32)
+    base = dict(cu_q=np.array([0, 1]), cu_k=np.array([0, L]), w=w,
+                q=np.zeros((T, 1, 8), np.float32), kv=np.zeros((L, 8), np.float32))
+    pmx = O.Problem(dict(base, q_idx=qc, k_idx=kc, q_scale=qs, k_scale=ks),
+                    idx_dtype="mxfp8", kv_dtype="f32", d_c=4, top_k=4)
+    # code · 2^k is exact in fp32 for these exponents
+    qf = (O.e4m3_to_f64(qc) * np.exp2(np.repeat(qs.astype(np.float64) - 127, 32, -1)))
+    kf = (O.e4m3_to_f64(kc) * np.exp2(np.repeat(ks.astype(np.float64) - 127, 32, -1)))
+    p32 = O.Problem(dict(base, q_idx=qf.astype(np.float32), k_idx=kf.astype(np.float32)),
+                    idx_dtype="f32", kv_dtype="f32", d_c=4, top_k=4)
+    assert np.array_equal(pmx.scores(0), p32.scores(0))
+
+
 # ---------------------------------------------------------------------------
 # Top-K.
 
