@@ -93,13 +93,14 @@ def positions(cfg):
 
 def work_model(cfg):
     """Algorithmic bytes and flops of each stage (what the method must move/compute)."""
-    es_i = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.idx_dtype]
+    es_i = {"f32": 4, "bf16": 2, "e4m3": 1, "mxfp8": 1}[cfg.idx_dtype]
     es_kv = {"f32": 4, "bf16": 2}[cfg.kv_dtype]
     es_o = {"f32": 4, "bf16": 2}[cfg.out_dtype]
     TQ, TK, D = cfg.total_q, cfg.total_k, cfg.d
     pairs = sum(p + 1 for p in positions(cfg))               # causal (query, key) pairs
     sel = sum(min(cfg.top_k, p + 1) for p in positions(cfg))  # selected (query, row) pairs
-    scales = (TK * 4 + TQ * cfg.h_idx * 4) if cfg.idx_dtype == "e4m3" else 0
+    scales = ((TK * 4 + TQ * cfg.h_idx * 4) if cfg.idx_dtype == "e4m3" else
+              (TK + TQ * cfg.h_idx) * (cfg.d_idx // 32) if cfg.idx_dtype == "mxfp8" else 0)
     idx_b = TQ * cfg.top_k * 4
     indexer_bytes = TK * cfg.d_idx * es_i + TQ * cfg.h_idx * (cfg.d_idx * es_i + 4) + scales + idx_b
     sfa_bytes = TQ * cfg.h * D * es_kv + sel * D * es_kv + idx_b + TQ * cfg.h * (cfg.d_c * es_o + 4)
@@ -116,7 +117,7 @@ def work_model(cfg):
 KERNEL_STAGE = {
     "indexer_scores_simt": "indexer", "indexer_tc_bf16": "indexer", "indexer_tc_fp8": "indexer",
     "indexer_tc_bf16_qb4": "indexer", "indexer_tc_fp8_qb4": "indexer",
-    "indexer_topk_bf16": "indexer", "indexer_topk_fp8": "indexer",
+    "indexer_topk_bf16": "indexer", "indexer_topk_fp8": "indexer", "indexer_tc_mxfp8": "indexer",
     "topk_rows": "topk", "topk_smem": "topk", "topk_stream": "topk",
     "sfa_simt": "sfa", "sfa_tc": "sfa",
 }
@@ -238,14 +239,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "tiny_prefill", "prefill_8k", "prefill_64k", "fp8_decode"])
+                    choices=["decode", "tiny_prefill", "prefill_8k", "prefill_64k", "fp8_decode",
+                             "mxfp8_decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=8, help="oracle rows per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="profiling: keep only the workload's first N sequences (same shapes)")
-    ap.add_argument("--extra", default="prefill_8k,fp8_decode,prefill_64k",
+    ap.add_argument("--extra", default="prefill_8k,fp8_decode,mxfp8_decode,prefill_64k",
                     help="other workloads timed after the primary one (N=1 only), reported "
                          "under \"workloads\"; empty for none")
     ap.add_argument("--page-size", type=int, default=0,
@@ -390,12 +392,13 @@ def main():
             extra[name] = {"value": ecfg.total_q * esteps / (etot / 1e3), "unit": "tokens/s",
                            "steps": esteps, "warmup": 3, "ms_per_step": etot / esteps,
                            "step_ms_median": statistics.median(ems), "workload": describe(ecfg),
-                           "dtype": ecfg.kv_dtype if ecfg.idx_dtype != "e4m3" else "e4m3+bf16",
+                           "dtype": (ecfg.kv_dtype if ecfg.idx_dtype not in ("e4m3", "mxfp8")
+                                     else ecfg.idx_dtype + "+bf16"),
                            "roofline": eroof, "kernels": ekern, "clocks": eclk,
                            "gpu_launches": len(erec)}
             del erun
             torch.cuda.empty_cache()
-            if ecfg.idx_dtype == "e4m3":
+            if ecfg.idx_dtype in ("e4m3", "mxfp8"):
                 extra[name]["topk_recall_vs_bf16"] = fp8_recall(dsa, W, ecfg,
                                                                 W.WORKLOAD_SEEDS[name], dev)
                 torch.cuda.empty_cache()
@@ -411,7 +414,8 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": cfg.kv_dtype if cfg.idx_dtype != "e4m3" else "e4m3+bf16",
+            "dtype": (cfg.kv_dtype if cfg.idx_dtype not in ("e4m3", "mxfp8")
+                      else cfg.idx_dtype + "+bf16"),
             "data": "synthetic (seeded N(0,1/sqrt(d)) values, w~U(0,1))",
             "config": {"workload": describe(cfg) + (f" paged={args.page_size}" if args.page_size
                                                     else ""),
@@ -443,19 +447,20 @@ def topk_recall(a, b):
 
 
 def fp8_recall(dsa, W, cfg, seed, dev, nseq=16):
-    """Top-K recall of the FP8 indexer against the bf16 indexer on the bf16 values it was
-    quantised from (the same seeded streams), over the workload's first nseq sequences."""
+    """Top-K recall of the quantised (FP8 or MXFP8) indexer against the bf16 indexer on the
+    bf16 values it was quantised from (the same seeded streams), over the workload's first
+    nseq sequences."""
     import dataclasses
     sub = W.first_sequences(cfg, nseq)
     res = {}
-    for dt in ("e4m3", "bf16"):
+    for dt in (cfg.idx_dtype, "bf16"):
         c = dataclasses.replace(sub, idx_dtype=dt)
         case = W.make_case(c, seed, attention=False)
         d = {k: v.to(dev) for k, v in case.tensors().items() if v.numel()}
         P = dsa.Problem.from_config(c, d["cu_q"], d["cu_k"])
         res[dt], _ = dsa.fused_indexer(P, d["q_idx"], d["k_idx"], d["w"], d.get("q_scale"),
                                        d.get("k_scale"))
-    r = topk_recall(res["e4m3"], res["bf16"])
+    r = topk_recall(res[cfg.idx_dtype], res["bf16"])
     return {"mean": float(r.mean()), "min": float(r.min()), "rows": int(r.numel()),
             "sample": f"the workload's first {nseq} sequences ({sub.total_k} keys)"}
 

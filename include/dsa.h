@@ -73,7 +73,8 @@ enum dsa_status {
 enum dsa_dtype {
   DSA_F32 = 0,       /* IEEE binary32 */
   DSA_BF16 = 1,      /* bfloat16 */
-  DSA_FP8_E4M3 = 2   /* OCP FP8 E4M3 ("fn": no infinities), with fp32 scales */
+  DSA_FP8_E4M3 = 2,  /* OCP FP8 E4M3 ("fn": no infinities), with fp32 scales */
+  DSA_MXFP8_E4M3 = 3 /* MXFP8: E4M3 codes with one E8M0 scale (2^(e-127)) per 32 elements */
 };
 
 /* Device status flags (bits of the workspace status word). */
@@ -103,7 +104,7 @@ typedef struct dsa_problem {
   int32_t d_c;         /* latent width = value width */
   int32_t d_rope;      /* rope width; a latent row has D = d_c + d_rope columns */
   int32_t top_k;       /* k: positions kept per query */
-  int32_t idx_dtype;   /* dsa_dtype of q_idx and k_idx (F32, BF16 or FP8_E4M3) */
+  int32_t idx_dtype;   /* dsa_dtype of q_idx and k_idx (F32, BF16, FP8_E4M3, MXFP8_E4M3) */
   int32_t kv_dtype;    /* dsa_dtype of q and kv (F32 or BF16) */
   int32_t out_dtype;   /* dsa_dtype of out (F32 or BF16) */
   float sm_scale;      /* softmax scale; 0 selects 1/sqrt(D) */
@@ -147,8 +148,14 @@ int dsa_workspace_size(const dsa_problem* p, int op, size_t* bytes);
  * k_idx  [total_k, d_idx]        idx_dtype
  * w      [total_q, h_idx]        f32 head weights
  * q_scale [total_q, h_idx] f32, k_scale [total_k] f32: dequantisation scales,
- *        required (and > 0) for FP8_E4M3, ignored (may be NULL) otherwise:
+ *        required (and > 0) for FP8_E4M3, ignored (may be NULL) for F32/BF16:
  *        q = code·q_scale[t,j], k = code·k_scale[s].
+ *        For MXFP8_E4M3 ("… New-Architecture LLMs" §5.1: index-side Q and K in
+ *        MXFP8, one scale per 32 elements; d_idx a multiple of 32) the same two
+ *        arguments point to E8M0 bytes instead: q_scale [total_q, h_idx, d_idx/32],
+ *        k_scale [total_k, d_idx/32] (paged like k_idx), and
+ *        q[t,j,c] = code·2^(q_scale[t,j,c/32] - 127), k[s,c] = code·2^(k_scale[s,c/32] - 127);
+ *        byte 255 (NaN) is not allowed.
  * scores [total_q, ld] f32, ld >= max_k_len.
  */
 int dsa_indexer_scores(const dsa_problem* p, const void* q_idx, const void* k_idx,

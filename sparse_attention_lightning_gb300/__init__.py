@@ -25,7 +25,8 @@ __all__ = ["Problem", "Workspace", "indexer_scores", "topk", "fused_indexer", "s
 
 _DT = {torch.float32: _abi.DSA_F32, torch.bfloat16: _abi.DSA_BF16,
        torch.uint8: _abi.DSA_FP8_E4M3, torch.float8_e4m3fn: _abi.DSA_FP8_E4M3}
-_NAME_DT = {"f32": _abi.DSA_F32, "bf16": _abi.DSA_BF16, "e4m3": _abi.DSA_FP8_E4M3}
+_NAME_DT = {"f32": _abi.DSA_F32, "bf16": _abi.DSA_BF16, "e4m3": _abi.DSA_FP8_E4M3,
+            "mxfp8": _abi.DSA_MXFP8_E4M3}
 _TORCH_OUT = {_abi.DSA_F32: torch.float32, _abi.DSA_BF16: torch.bfloat16}
 
 
@@ -190,9 +191,15 @@ def _need(t: Optional[torch.Tensor], name: str, dtype_code: Optional[int], shape
 
 
 def _check_indexer(P: Problem, q_idx, k_idx, w, q_scale, k_scale):
-    _need(q_idx, "q_idx", P.idx_dtype, (P.total_q, P.h_idx, P.d_idx))
-    _need(k_idx, "k_idx", P.idx_dtype, (P.cache_rows, P.d_idx))
+    mx = P.idx_dtype == _abi.DSA_MXFP8_E4M3
+    codes = _abi.DSA_FP8_E4M3 if mx else P.idx_dtype  # MXFP8 codes are E4M3 bytes
+    _need(q_idx, "q_idx", codes, (P.total_q, P.h_idx, P.d_idx))
+    _need(k_idx, "k_idx", codes, (P.cache_rows, P.d_idx))
     _need(w, "w", _abi.DSA_F32, (P.total_q, P.h_idx))
+    if mx:  # E8M0 bytes, one per 32 elements
+        _need(q_scale, "q_scale", _abi.DSA_FP8_E4M3, (P.total_q, P.h_idx, P.d_idx // 32))
+        _need(k_scale, "k_scale", _abi.DSA_FP8_E4M3, (P.cache_rows, P.d_idx // 32))
+        return
     fp8 = P.idx_dtype == _abi.DSA_FP8_E4M3
     _need(q_scale, "q_scale", _abi.DSA_F32, (P.total_q, P.h_idx), optional=not fp8)
     _need(k_scale, "k_scale", _abi.DSA_F32, (P.cache_rows,), optional=not fp8)

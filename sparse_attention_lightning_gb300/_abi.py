@@ -9,7 +9,7 @@ LIB_PATH = os.path.join(_PKG, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_WORKSPACE, \
     DSA_ERR_TIMEOUT = range(6)
-DSA_F32, DSA_BF16, DSA_FP8_E4M3 = 0, 1, 2
+DSA_F32, DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2, 3
 DSA_FLAG_BAD_INDEX, DSA_FLAG_BAD_SEQS, DSA_FLAG_TIMEOUT = 0x1, 0x2, 0x4
 OP_INDEXER_SCORES, OP_TOPK, OP_FUSED_INDEXER, OP_SPARSE_MLA_ATTN, OP_FUSED_FORWARD = 1, 2, 3, 4, 5
 

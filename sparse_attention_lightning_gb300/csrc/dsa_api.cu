@@ -170,8 +170,12 @@ int check_problem(const dsa_problem* p, bool need_indexer, bool need_attn) {
     if (p->d_idx < 16 || p->d_idx > 256 || p->d_idx % 16)
       return set_error(DSA_ERR_UNSUPPORTED, "d_idx = %d (supported 16..256, multiple of 16)",
                        p->d_idx);
-    if (p->idx_dtype != DSA_F32 && p->idx_dtype != DSA_BF16 && p->idx_dtype != DSA_FP8_E4M3)
+    if (p->idx_dtype != DSA_F32 && p->idx_dtype != DSA_BF16 && p->idx_dtype != DSA_FP8_E4M3 &&
+        p->idx_dtype != DSA_MXFP8_E4M3)
       return set_error(DSA_ERR_INVALID_ARG, "idx_dtype = %d", p->idx_dtype);
+    if (p->idx_dtype == DSA_MXFP8_E4M3 && p->d_idx % 32)
+      return set_error(DSA_ERR_UNSUPPORTED, "MXFP8 needs d_idx a multiple of 32 (d_idx = %d)",
+                       p->d_idx);
   }
   if (need_attn) {
     if (p->h < 1 || p->h > 128) return set_error(DSA_ERR_UNSUPPORTED, "h = %d (1..128)", p->h);
@@ -221,7 +225,7 @@ size_t idx_bytes(const dsa_problem* p) { return (size_t)p->total_q * p->top_k * 
 IndexerArgs indexer_args(const dsa_problem* p, const void* q_idx, const void* k_idx,
                          const float* w, const float* q_scale, const float* k_scale,
                          void* ws) {
-  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3;
+  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3 || p->idx_dtype == DSA_MXFP8_E4M3;
   return IndexerArgs{seqs_of(p), p->h_idx, p->d_idx, p->idx_dtype, q_idx, k_idx, w,
                      fp8 ? q_scale : nullptr, fp8 ? k_scale : nullptr,
                      static_cast<uint32_t*>(ws)};
@@ -328,7 +332,7 @@ int check_indexer_inputs(const dsa_problem* p, const void* q_idx, const void* k_
   DSA_TRY(check_ptr(q_idx, "q_idx", p->total_q == 0));
   DSA_TRY(check_ptr(k_idx, "k_idx"));
   DSA_TRY(check_ptr(w, "w", p->total_q == 0));
-  if (p->idx_dtype == DSA_FP8_E4M3) {
+  if (p->idx_dtype == DSA_FP8_E4M3 || p->idx_dtype == DSA_MXFP8_E4M3) {
     DSA_TRY(check_ptr(q_scale, "q_scale", p->total_q == 0));
     DSA_TRY(check_ptr(k_scale, "k_scale"));
   }

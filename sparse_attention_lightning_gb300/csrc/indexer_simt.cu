@@ -10,7 +10,8 @@
 // One CTA = one query row × one tile of 64 keys.  The query row (H_I × d_I) and
 // the key tile sit in shared memory as fp32 (FP8 dequantised on load); each of
 // the 256 threads takes one key and a quarter of the heads, and the four
-// partial head sums are added in a fixed order.
+// partial head sums are added in a fixed order.  MXFP8 inputs are dequantised
+// with their E8M0 group scale (one per 32 elements of a query head or a key).
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -37,11 +38,16 @@ indexer_scores_simt_kernel(IndexerArgs a, float* __restrict__ scores, int64_t ld
   const TI* qg = static_cast<const TI*>(a.q_idx) + (int64_t)t * HI * DI;
   const TI* kg = static_cast<const TI*>(a.k_idx);
   const bool fp8 = a.q_scale != nullptr;
+  const bool mx = a.idx_dtype == DSA_MXFP8_E4M3;
+  const int G = DI / 32;  // MXFP8 scale groups per head / key
+  const uint8_t* qsb = reinterpret_cast<const uint8_t*>(a.q_scale);
+  const uint8_t* ksb = reinterpret_cast<const uint8_t*>(a.k_scale);
 
   // the query row and its head weights
   for (int i = tid; i < HI * DI; i += kThreads) {
     float v = to_f32(qg[i]);
-    if (fp8) v *= __ldg(a.q_scale + (int64_t)t * HI + i / DI);
+    if (mx) v *= e8m0_to_f32(__ldg(qsb + ((int64_t)t * HI + i / DI) * G + (i % DI) / 32));
+    else if (fp8) v *= __ldg(a.q_scale + (int64_t)t * HI + i / DI);
     qs[i] = v;
   }
   for (int j = tid; j < HI; j += kThreads) wsm[j] = __ldg(a.w + (int64_t)t * HI + j);
@@ -62,7 +68,8 @@ indexer_scores_simt_kernel(IndexerArgs a, float* __restrict__ scores, int64_t ld
         const int64_t row = (int64_t)key_row(a.seqs, r.b, r.k0, (int)s);  // -1: page outside the cache
         if (row >= 0) {
           v = to_f32(kg[row * DI + c]);
-          if (fp8) v *= __ldg(a.k_scale + row);
+          if (mx) v *= e8m0_to_f32(__ldg(ksb + row * G + c / 32));
+          else if (fp8) v *= __ldg(a.k_scale + row);
         } else if (c == 0) {
           atomicOr(a.status, DSA_FLAG_BAD_SEQS);
         }
@@ -117,7 +124,8 @@ int launch_indexer_scores_simt(const IndexerArgs& a, float* scores, int64_t ld,
   switch (a.idx_dtype) {
     case DSA_F32: return launch_typed<float>(a, scores, ld, stream);
     case DSA_BF16: return launch_typed<__nv_bfloat16>(a, scores, ld, stream);
-    case DSA_FP8_E4M3: return launch_typed<__nv_fp8_e4m3>(a, scores, ld, stream);
+    case DSA_FP8_E4M3:
+    case DSA_MXFP8_E4M3: return launch_typed<__nv_fp8_e4m3>(a, scores, ld, stream);
   }
   return set_error(DSA_ERR_UNSUPPORTED, "indexer: idx_dtype %d", a.idx_dtype);
 }

@@ -17,6 +17,11 @@
 // reads its key's 64 columns and reduces them to one score (ReLU, · w, Σ_j)
 // without any cross-thread reduction.  For FP8 the scales fold in as
 // I = k_scale[s] · Σ_j (w·q_scale)[t,j] · ReLU(z8) (all scales are positive).
+// MXFP8 (one E8M0 scale per 32 elements of a head or key; "… New-Architecture
+// LLMs" §5.1) cannot fold a scale past the sum over d_I, so each of a tile's four
+// K = 32 MMAs writes its own accumulator (4 × 64 columns, double buffered: all 512)
+// and the epilogue forms z_j = Σ_g 2^(ek_g) 2^(eq_jg) z_jg before the ReLU, two heads
+// at a time with packed fp32x2 arithmetic (QB = 1 only).
 //
 // Schedule: the tiles of all blocks are laid end to end (a block whose last row
 // sits at position p has floor(p/128) + 1 of them) and each persistent CTA takes
@@ -43,8 +48,9 @@ using namespace sched;
 
 constexpr int kMaxSeqs = 4096;  // sequences per launch on this path (tile table in smem)
 
-template <bool FP8, int QB>
+template <bool FP8, int QB, bool MX = false>
 struct Cfg {
+  static_assert(!MX || (FP8 && QB == 1), "MXFP8 runs with one query row per block");
   static constexpr int BM = 128;   // keys per tile (MMA M)
   static constexpr int HI = 64;    // heads per query row
   static constexpr int N = HI * QB;  // MMA N: the block's heads
@@ -57,7 +63,7 @@ struct Cfg {
   static constexpr int NQ = QB == 1 ? 2 : 1;       // query-block buffers
   static constexpr int NS = QB == 1 ? (FP8 ? 8 : 4) : (FP8 ? 6 : 3);  // key-tile stages
   static constexpr int KSTEPS = FP8 ? 4 : 8;       // MMAs per tile (32 B of K each)
-  static constexpr int ACC_COLS = N;               // fp32 accumulator columns
+  static constexpr int ACC_COLS = MX ? 4 * N : N;  // fp32 accumulator columns (MX: per group)
   static constexpr int TMEM_COLS = 2 * ACC_COLS;   // double buffered
   static constexpr int EPI_WARPS = 8;
   // QB = 1: two groups of four warps take alternate tiles (group g owns accumulator g), so
@@ -77,7 +83,9 @@ struct Cfg {
   static constexpr int SC_BOX = BM + 4;
   static constexpr int SC_BYTES = SC_BOX * 4;      // 528 bytes a box
   static constexpr int SC_SLOT = 640;              // slot stride (128-byte aligned copies)
-  static constexpr int MISC = 512 /*barriers*/ + EPI_WARPS * RPW * HI * 4 /*weights*/ + 64;
+  static constexpr int SQ_FLOATS = MX ? HI * 4 : 0;  // MX: per warp, the row's group scales
+  static constexpr int MISC = 512 /*barriers*/ + EPI_WARPS * RPW * HI * 4 /*weights*/ +
+                              EPI_WARPS * SQ_FLOATS * 4 + 64;
   static constexpr int SMEM_FIXED =
       NS * KTILE + NQ * QTILE + HIST_BYTES + NSC * SC_SLOT + MISC + 1024 /*align*/;
   static_assert(TMEM_COLS <= 512, "TMEM");
@@ -120,11 +128,25 @@ __device__ __forceinline__ uint32_t scan_block(uint32_t v, uint32_t* ws, uint32_
   return before + x - v;
 }
 
-template <bool FP8, int QB>
-__global__ void __launch_bounds__(Cfg<FP8, QB>::THREADS, 1)
+// Four 16-column TMEM loads of this warp's 32 lanes, `stride` columns apart (the four MXFP8
+// group accumulators of 16 heads), then one wait.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t taddr, uint32_t stride, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride), "r"(taddr + 3 * stride)
+      : "memory");
+}
+
+template <bool FP8, int QB, bool MX>
+__global__ void __launch_bounds__(Cfg<FP8, QB, MX>::THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const __grid_constant__ CUtensorMap smap, Params p) {
-  using C = Cfg<FP8, QB>;
+  using C = Cfg<FP8, QB, MX>;
   static_assert(2 * C::NS + 4 + 4 + 3 + C::NSC <= 64, "barrier area");
   constexpr int NSCM = C::NSC > 0 ? C::NSC : 1;  // scale slots (as a modulus)
   constexpr int EPI_THREADS = 32 * C::EPI_WARPS;
@@ -146,7 +168,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   uint64_t* epi_b = drain + 2;     // the epilogue threads: histograms flushed
   uint64_t* sc_empty = drain + 3;  // [NSC] FP8: the tile's epilogue warps have read its scales
   float* wsm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);  // [warps][RPW][64]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wsm + C::EPI_WARPS * C::RPW * C::HI);
+  // MX: [warps][32 head pairs][4 groups] float2 (heads 2i, 2i+1 of a group side by side)
+  float4* sqm = reinterpret_cast<float4*>(wsm + C::EPI_WARPS * C::RPW * C::HI);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(wsm + C::EPI_WARPS * C::RPW * C::HI + C::EPI_WARPS * C::SQ_FLOATS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* scan_ws = tmem_slot + 2;                   // [THREADS / 32]
   int32_t* tab = reinterpret_cast<int32_t*>(smem + C::SMEM_FIXED - 1024);
@@ -308,7 +333,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           const int atom = (kk * 32) / 128, off = (kk * 32) % 128;
           const uint64_t ad = sdesc_sw128(a0 + atom * (C::BM * 128) + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(b0 + atom * (C::N * 128) + off, 16, 1024);
-          if (FP8) mma_e4m3(tmem + acc * C::ACC_COLS, ad, bd, idesc, kk > 0);
+          if (MX) mma_e4m3(tmem + acc * C::ACC_COLS + kk * C::N, ad, bd, idesc, false);
+          else if (FP8) mma_e4m3(tmem + acc * C::ACC_COLS, ad, bd, idesc, kk > 0);
           else mma_bf16(tmem + acc * C::ACC_COLS, ad, bd, idesc, kk > 0);
         }
         mma_commit(&k_empty[s]);
@@ -341,9 +367,19 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           const int64_t t = cur.t + (r < cur.nrow ? r : 0);
           float w0 = __ldg(p.w + t * C::HI + lane);
           float w1 = __ldg(p.w + t * C::HI + lane + 32);
-          if (FP8) {
+          if (FP8 && !MX) {
             w0 *= __ldg(p.q_scale + t * C::HI + lane);
             w1 *= __ldg(p.q_scale + t * C::HI + lane + 32);
+          }
+          if (MX) {
+            // heads 2·lane and 2·lane + 1: their four E8M0 group scales, paired per group
+            const uint32_t* qb = reinterpret_cast<const uint32_t*>(p.q_scale) + t * C::HI;
+            const uint32_t a0 = __ldg(qb + 2 * lane), a1 = __ldg(qb + 2 * lane + 1);
+            float4* d = sqm + ew * (C::SQ_FLOATS / 4) + 2 * lane;
+            d[0] = make_float4(e8m0_to_f32(a0 & 0xff), e8m0_to_f32(a1 & 0xff),
+                               e8m0_to_f32((a0 >> 8) & 0xff), e8m0_to_f32((a1 >> 8) & 0xff));
+            d[1] = make_float4(e8m0_to_f32((a0 >> 16) & 0xff), e8m0_to_f32((a1 >> 16) & 0xff),
+                               e8m0_to_f32(a0 >> 24), e8m0_to_f32(a1 >> 24));
           }
           wq[rr * C::HI + lane] = w0;
           wq[rr * C::HI + lane + 32] = w1;
@@ -374,20 +410,59 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                              rgrp * C::RPW * C::HI;
       // Σ_j w_j · ReLU(z_j) as four interleaved partial sums (a short dependency chain)
       float sum[C::RPW];
+      if (MX) {
+        // this key's four group scales (one 4-byte word in the scale ring), each paired
+        float2 ek[4];
+        const uint32_t kb = __float_as_uint(ksc);
 #pragma unroll
-      for (int rr = 0; rr < C::RPW; ++rr) {
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int g = 0; g < 4; ++g) {
+          const float f = e8m0_to_f32((kb >> (8 * g)) & 0xff);
+          ek[g] = make_float2(f, f);
+        }
+        const float4* sq = sqm + ew * (C::SQ_FLOATS / 4);
+        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t r[32];
-          tmem_ld32(taddr + rr * C::HI + 32 * h2, r);
+        for (int hc = 0; hc < C::HI / 16; ++hc) {
+          uint32_t r[64];  // groups 0..3 of heads 16·hc .. 16·hc + 15
+          tmem_ld16x4(taddr + 16 * hc, C::N, r);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const float wj = QB == 1 ? wreg[32 * h2 + jj] : wq[rr * C::HI + 32 * h2 + jj];
-            part[jj & 3] = fmaf(wj, fmaxf(__uint_as_float(r[jj]), 0.f), part[jj & 3]);
+          for (int q2 = 0; q2 < 8; ++q2) {
+            const int jp = 8 * hc + q2;  // head pair: heads 2·jp, 2·jp + 1
+            const float4 s01 = sq[2 * jp], s23 = sq[2 * jp + 1];
+            const float2 c0 = __fmul2_rn(ek[0], make_float2(s01.x, s01.y));
+            const float2 c1 = __fmul2_rn(ek[1], make_float2(s01.z, s01.w));
+            const float2 c2 = __fmul2_rn(ek[2], make_float2(s23.x, s23.y));
+            const float2 c3 = __fmul2_rn(ek[3], make_float2(s23.z, s23.w));
+            float2 z = __fmul2_rn(c0, make_float2(__uint_as_float(r[2 * q2]),
+                                                  __uint_as_float(r[2 * q2 + 1])));
+            z = __ffma2_rn(c1, make_float2(__uint_as_float(r[16 + 2 * q2]),
+                                           __uint_as_float(r[16 + 2 * q2 + 1])), z);
+            z = __ffma2_rn(c2, make_float2(__uint_as_float(r[32 + 2 * q2]),
+                                           __uint_as_float(r[32 + 2 * q2 + 1])), z);
+            z = __ffma2_rn(c3, make_float2(__uint_as_float(r[48 + 2 * q2]),
+                                           __uint_as_float(r[48 + 2 * q2 + 1])), z);
+            const float2 wp = make_float2(wreg[2 * jp], wreg[2 * jp + 1]);
+            part[q2 & 1] = __ffma2_rn(wp, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)),
+                                      part[q2 & 1]);
           }
         }
-        sum[rr] = (part[0] + part[1]) + (part[2] + part[3]);
+        sum[0] = (part[0].x + part[1].x) + (part[0].y + part[1].y);
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < C::RPW; ++rr) {
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t r[32];
+            tmem_ld32(taddr + rr * C::HI + 32 * h2, r);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const float wj = QB == 1 ? wreg[32 * h2 + jj] : wq[rr * C::HI + 32 * h2 + jj];
+              part[jj & 3] = fmaf(wj, fmaxf(__uint_as_float(r[jj]), 0.f), part[jj & 3]);
+            }
+          }
+          sum[rr] = (part[0] + part[1]) + (part[2] + part[3]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -398,7 +473,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int r = rgrp * C::RPW + rr;  // the same in the whole warp
         const bool valid = r < cur.nrow && s <= cur.pos + r;
         float v = sum[rr];
-        if (FP8) v *= ksc;
+        if (FP8 && !MX) v *= ksc;
         if (valid) p.scores[(int64_t)(cur.t + r - p.r0) * p.ld + s] = v;
         if (p.hist) {
           // scores of neighbouring keys share bins: one shared-memory atomic per bin per warp
@@ -451,9 +526,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
 }
 
-template <bool FP8, int QB>
+template <bool FP8, int QB, bool MX = false>
 int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
-  using C = Cfg<FP8, QB>;
+  using C = Cfg<FP8, QB, MX>;
   CUtensorMap kmap, qmap, smap;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int cr = tile_chunk_rows(a.seqs);  // key rows per copy (a page, for small pages)
@@ -464,7 +539,8 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
                     128 / C::ES, C::N);
   if (rc != DSA_OK) return rc;
   if (FP8) {
-    // k_scale as one row of total_k floats (no swizzle), read in boxes of 132
+    // k_scale as one row of total_k 4-byte words (no swizzle), read in boxes of 132: an fp32
+    // scale per key, or (MX) a key's four E8M0 group scales
     const uint64_t rows = (uint64_t)a.seqs.cache_rows();
     rc = make_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, rows, 1,
                       align_up((size_t)rows * 4, 16), a.seqs.paged() ? (uint32_t)cr : C::SC_BOX,
@@ -474,7 +550,7 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
     smap = kmap;  // unused
   }
   const int smem = C::SMEM_FIXED + (int)align_up(3 * sizeof(int32_t) * (a.seqs.B + 1), 16);
-  auto kern = indexer_tc_kernel<FP8, QB>;
+  auto kern = indexer_tc_kernel<FP8, QB, MX>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return check_launch("indexer_tc: smem attribute");
   const int r1 = a.row1 < a.seqs.total_q ? a.row1 : a.seqs.total_q;
@@ -482,8 +558,9 @@ int launch_typed(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t s
   const int64_t bound = (int64_t)(r1 - a.row0) * ((a.seqs.max_k_len + C::BM - 1) / C::BM);
   const int grid = (int)(bound < num_sms() ? bound : num_sms());
   Params p{a.seqs, a.w, a.q_scale, a.k_scale, scores, ld, a.status, a.hist, a.row0, r1};
-  DSA_LAUNCH(FP8 ? (QB == 1 ? "indexer_tc_fp8" : "indexer_tc_fp8_qb4")
-                 : (QB == 1 ? "indexer_tc_bf16" : "indexer_tc_bf16_qb4"),
+  DSA_LAUNCH(MX ? "indexer_tc_mxfp8"
+             : FP8 ? (QB == 1 ? "indexer_tc_fp8" : "indexer_tc_fp8_qb4")
+                   : (QB == 1 ? "indexer_tc_bf16" : "indexer_tc_bf16_qb4"),
              stream, kern<<<grid, C::THREADS, smem, stream>>>(kmap, qmap, smap, p));
   return check_launch("indexer_tc");
 }
@@ -494,9 +571,10 @@ bool indexer_tc_eligible(const IndexerArgs& a) {
   // tiles of the whole problem must stay below 2^31 (int32 item indices)
   const int64_t bound = (int64_t)a.seqs.total_q * ((a.seqs.max_k_len + 127) / 128);
   // (FP8: the key scales are read by TMA, which wants a 16-byte aligned base)
-  return (a.idx_dtype == DSA_BF16 || a.idx_dtype == DSA_FP8_E4M3) && a.h_idx == 64 &&
-         a.d_idx == 128 && a.seqs.B <= kMaxSeqs && bound < (int64_t(1) << 31) &&
-         (a.idx_dtype != DSA_FP8_E4M3 || (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0);
+  const bool q8 = a.idx_dtype == DSA_FP8_E4M3 || a.idx_dtype == DSA_MXFP8_E4M3;
+  return (a.idx_dtype == DSA_BF16 || q8) && a.h_idx == 64 && a.d_idx == 128 &&
+         a.seqs.B <= kMaxSeqs && bound < (int64_t(1) << 31) &&
+         (!q8 || (reinterpret_cast<uintptr_t>(a.k_scale) & 15) == 0);
 }
 
 // blocks of four query rows when sequences hold several queries each (prefill)
@@ -507,6 +585,8 @@ bool indexer_tc_blocks4(const IndexerArgs& a) {
 int launch_indexer_tc(const IndexerArgs& a, float* scores, int64_t ld, cudaStream_t stream) {
   if (a.seqs.total_q == 0) return DSA_OK;
   const bool qb4 = indexer_tc_blocks4(a);
+  // MXFP8 keeps four accumulators per tile, which leaves TMEM room for one query row per block
+  if (a.idx_dtype == DSA_MXFP8_E4M3) return launch_typed<true, 1, true>(a, scores, ld, stream);
   if (a.idx_dtype == DSA_FP8_E4M3)
     return qb4 ? launch_typed<true, 4>(a, scores, ld, stream)
                : launch_typed<true, 1>(a, scores, ld, stream);

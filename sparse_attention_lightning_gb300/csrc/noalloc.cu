@@ -71,7 +71,7 @@ extern "C" int dsa_fused_indexer_static(const dsa_problem* p, const void* q_idx,
                      "dsa_fused_indexer_static: total_q*max_k_len = %zu exceeds the static "
                      "scratch of %zu scores",
                      need, kStaticScoreFloats);
-  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3;
+  const bool fp8 = p->idx_dtype == DSA_FP8_E4M3 || p->idx_dtype == DSA_MXFP8_E4M3;
   const bool none = p->total_q == 0;
   if ((!q_idx && !none) || !k_idx || (!w && !none) || (!idx && !none))
     return set_error(DSA_ERR_INVALID_ARG, "a required pointer is NULL");

@@ -18,6 +18,10 @@ bf16 8k prefill, bf16 64k prefill, FP8-indexer decode):
 * FP8 indexer inputs: bf16-valued data quantised per token (one fp32 scale
   per key row, one per query token broadcast over its heads), scale =
   amax/448, codes = E4M3 round-to-nearest-even of x/scale;
+* MXFP8 indexer inputs: the same bf16 draws quantised per 32 elements: the
+  shared scale 2^e is the smallest power of two with amax / 2^e <= 448 (so no
+  element saturates), stored as the E8M0 byte e + 127 (127 for an all-zero
+  group), codes = E4M3 round-to-nearest-even of x / 2^e;
 * indexer prolog inputs (``prolog_inputs``): the bf16 indexer query before
   quantisation (the same draw the FP8 query codes are made from), a hidden
   state ``x[ΣT, d_model]`` ~ N(0, 1) and a head-weight projection
@@ -33,12 +37,13 @@ from typing import Dict, List, Optional, Sequence
 
 import torch
 
-F32, BF16, FP8 = "f32", "bf16", "e4m3"
+F32, BF16, FP8, MXFP8 = "f32", "bf16", "e4m3", "mxfp8"
 
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
 # Stable ids so each tensor gets its own stream for a given seed.
-_STREAM_IDS = {"lens": 1, "q_idx": 2, "k_idx": 3, "w": 4, "q": 5, "kv": 6, "x": 7, "w_h": 8}
+_STREAM_IDS = {"lens": 1, "q_idx": 2, "k_idx": 3, "w": 4, "q": 5, "kv": 6, "x": 9, "w_h": 10}
+# (7 is the page order of paged caches)
 
 _CHUNK = 1 << 24  # values drawn per generator call (bounds host temporaries)
 
@@ -81,7 +86,8 @@ class Config:
 class Case:
     """Host tensors of one problem.
 
-    FP8 tensors are stored as their raw E4M3 code bytes (``torch.uint8``).
+    FP8 tensors are stored as their raw E4M3 code bytes (``torch.uint8``); MXFP8 scales as
+    their E8M0 bytes.
     """
 
     cfg: Config
@@ -92,7 +98,7 @@ class Case:
     w: torch.Tensor
     q: torch.Tensor
     kv: torch.Tensor
-    q_scale: Optional[torch.Tensor] = None  # f32 [ΣT, H_I] (FP8 only)
+    q_scale: Optional[torch.Tensor] = None  # f32 [ΣT, H_I] (FP8); uint8 [ΣT, H_I, d_I/32] (MXFP8)
     k_scale: Optional[torch.Tensor] = None  # f32 [ΣL] (FP8 only)
 
     def tensors(self) -> Dict[str, torch.Tensor]:
@@ -135,6 +141,20 @@ def _quantise_e4m3_rows(x: torch.Tensor):
     return codes, scale.contiguous()
 
 
+def _quantise_mx_rows(x: torch.Tensor):
+    """E4M3 codes [R, n] and E8M0 scale bytes [R, n/32] of a 2-D tensor, one scale per 32
+    consecutive elements (input preparation)."""
+    R, n = x.shape
+    xf = x.to(torch.float32).reshape(R, n // 32, 32)
+    amax = xf.abs().amax(dim=2)
+    m, ex = torch.frexp(amax)                   # amax = m·2^ex, m in [0.5, 1); 448 = 0.875·2^9
+    e = ex - 9 + (m > 0.875).to(ex.dtype)       # smallest e with amax <= 448·2^e
+    e = torch.where(amax > 0, e, torch.zeros_like(e)).clamp_(-127, 127)
+    y = (xf / torch.exp2(e.to(torch.float32))[:, :, None]).clamp_(-448.0, 448.0)
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(R, n)
+    return codes, (e + 127).to(torch.uint8).contiguous()
+
+
 def decode_lengths(batch: int, lo: int, hi: int, seed: int) -> List[int]:
     """Context lengths integer-uniform in [lo, hi], inclusive."""
     g = _gen(seed, "lens")
@@ -165,6 +185,13 @@ def make_case(cfg: Config, seed: int, attention: bool = True) -> Case:
         q_idx = q_codes.view(TQ, cfg.h_idx, cfg.d_idx)
         q_scale = qs[:, None].expand(TQ, cfg.h_idx).contiguous()
         k_idx, k_scale = _quantise_e4m3_rows(kf)
+    elif cfg.idx_dtype == MXFP8:
+        qf = _normal((TQ, cfg.h_idx * cfg.d_idx), sd_i, _gen(seed, "q_idx"), torch.bfloat16)
+        kf = _normal((TK, cfg.d_idx), sd_i, _gen(seed, "k_idx"), torch.bfloat16)
+        q_codes, qs = _quantise_mx_rows(qf.reshape(TQ * cfg.h_idx, cfg.d_idx))
+        q_idx = q_codes.view(TQ, cfg.h_idx, cfg.d_idx)
+        q_scale = qs.view(TQ, cfg.h_idx, cfg.d_idx // 32)
+        k_idx, k_scale = _quantise_mx_rows(kf)
     else:
         idd = _TORCH_DTYPE[cfg.idx_dtype]
         q_idx = _normal((TQ, cfg.h_idx, cfg.d_idx), sd_i, _gen(seed, "q_idx"), idd)
@@ -202,8 +229,14 @@ def fp8_decode(batch: int = 128, L: int = 131072) -> Config:
                   64, 2048, FP8, BF16, BF16)
 
 
+def mxfp8_decode(batch: int = 128, L: int = 131072) -> Config:
+    """The FP8 indexer decode shape with the pages' MXFP8 index format (same bf16 draws)."""
+    return Config(f"mxfp8_indexer_decode_B{batch}_L{L}", [1] * batch, [L] * batch, 64, 128, 128,
+                  512, 64, 2048, MXFP8, BF16, BF16)
+
+
 WORKLOAD_SEEDS = {"tiny_prefill": 0, "decode": 1, "prefill_8k": 2, "prefill_64k": 3,
-                  "fp8_decode": 4}
+                  "fp8_decode": 4, "mxfp8_decode": 4}
 
 
 def workload(name: str) -> Config:
@@ -217,6 +250,8 @@ def workload(name: str) -> Config:
         return prefill(65536)
     if name == "fp8_decode":
         return fp8_decode()
+    if name == "mxfp8_decode":
+        return mxfp8_decode()
     raise KeyError(name)
 
 
@@ -241,7 +276,7 @@ class PagedKeys:
     block_table: torch.Tensor   # int32 [B, max_pages]: page of each sequence's page slot, -1 unused
     k_idx: torch.Tensor         # [num_pages * page_size, d_I]
     kv: torch.Tensor            # [num_pages * page_size, D]
-    k_scale: Optional[torch.Tensor] = None  # f32 [num_pages * page_size] (FP8 only)
+    k_scale: Optional[torch.Tensor] = None  # [num_pages * page_size] f32 (FP8), [.., d_I/32] uint8 (MXFP8)
 
     def tensors(self) -> Dict[str, torch.Tensor]:
         out = {"block_table": self.block_table, "k_idx": self.k_idx, "kv": self.kv}
@@ -283,7 +318,10 @@ def paged_keys(case: Case, page_size: int, seed: int, spare_pages: int = 3) -> P
         return out
 
     fill_idx = 0x7E if case.k_idx.dtype == torch.uint8 else 100.0  # E4M3 code 0x7E = 448
-    k_scale = scatter(case.k_scale, 1.0e4) if case.k_scale is not None else None
+    if case.k_scale is None:
+        k_scale = None
+    else:
+        k_scale = scatter(case.k_scale, 200 if case.k_scale.dtype == torch.uint8 else 1.0e4)
     return PagedKeys(page_size, num_pages, table, scatter(case.k_idx, fill_idx),
                      scatter(case.kv, 100.0), k_scale)
 

@@ -25,7 +25,7 @@ TOL = {
 
 
 def tol_for(cfg):
-    if cfg.idx_dtype == "e4m3":
+    if cfg.idx_dtype in ("e4m3", "mxfp8"):  # quantised indexer configurations
         return TOL["e4m3"]
     return TOL["f32"] if (cfg.kv_dtype == "f32" and cfg.out_dtype == "f32") else TOL["bf16"]
 

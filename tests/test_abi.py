@@ -72,6 +72,13 @@ def test_descriptor_checks(L, field, value, code):
     assert L.dsa_last_error()
 
 
+def test_mxfp8_descriptor(L):
+    # MXFP8 scales cover 32 elements: d_idx must be a multiple of 32
+    assert _ws_size(L, _problem(idx_dtype=_abi.DSA_MXFP8_E4M3, d_idx=64), 5)[0] == 0
+    assert _ws_size(L, _problem(idx_dtype=_abi.DSA_MXFP8_E4M3, d_idx=48), 5)[0] == \
+        _abi.DSA_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(page_size=48, max_pages=2, num_pages=4, block_table=1 << 16), _abi.DSA_ERR_UNSUPPORTED),
     (dict(page_size=384, max_pages=1, num_pages=4, block_table=1 << 16), _abi.DSA_ERR_UNSUPPORTED),
