@@ -42,16 +42,21 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     # (kernel, workload): (bytes per launch, sources, sha256 prefix of the sources); a kernel
     # whose sources changed since the capture reports null (profiles/ has the captures)
-    ("indexer_topk_bf16", "decode"): (179_345_664, ("indexer_topk.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "4347068d89e8dea2"),
-    ("sfa_tc", "decode"): (83_910_400, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "203efdfbc5fe2ea1"),
-    ("sfa_tc", "prefill_8k"): (2_322_682_624, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "203efdfbc5fe2ea1"),
-    ("topk_stream", "prefill_8k"): (33_485_056, ("topk_stream.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "2b1df69854b37618"),
-    ("indexer_tc_bf16_qb4", "prefill_8k"): (58_224_640, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "c4b82c62c6fd0a83"),
+    ("indexer_topk_bf16", "decode"): (179_346_944, ("indexer_topk.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "d9eb93a069b24d06"),
+    ("sfa_tc", "decode"): (83_959_808, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "b1b19e5969abc2a5"),
+    ("sfa_tc", "prefill_8k"): (2_323_838_976, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "b1b19e5969abc2a5"),
+    ("topk_stream", "prefill_8k"): (33_478_400, ("topk_stream.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "a77d9d9321f97c28"),
+    ("indexer_tc_bf16_qb4", "prefill_8k"): (58_037_248, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "51f180f72387c469"),
+    # captured on the workload's first 16 of 128 sequences (--batch 16) and scaled by 8: the
+    # key codes and their scales, read once, are 99 % of it and grow with the keys
+    ("indexer_tc_mxfp8", "mxfp8_decode"): (2_252_701_696, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "51f180f72387c469"),
+    ("indexer_prolog", "decode"): (1_932_800, ("prolog.cu", "dsa_internal.cuh"), "c6a5a8bce52afac8"),
 }
 
 
@@ -405,8 +410,8 @@ def main():
         # the indexer prolog (Q quantisation + head-weight projection, one launch) on the
         # query batches of the two decode workloads
         extra["indexer_prolog"] = {
-            name: prolog_record(dsa, W, torch, dist, dev, local, W.workload(name),
-                                W.WORKLOAD_SEEDS[name], max(3, args.steps // 4))
+            name: prolog_record(dsa, W, torch, dist, dev, local, name, W.WORKLOAD_SEEDS[name],
+                                max(3, args.steps // 4))
             for name in ("decode", "fp8_decode")}
 
     if rank == 0:
@@ -465,11 +470,11 @@ def fp8_recall(dsa, W, cfg, seed, dev, nseq=16):
             "sample": f"the workload's first {nseq} sequences ({sub.total_k} keys)"}
 
 
-def prolog_record(dsa, W, torch, dist, dev, local, cfg, seed, steps):
-    """The indexer prolog on ``cfg``'s query tokens: timed like a step (L2 flushed before
+def prolog_record(dsa, W, torch, dist, dev, local, name, seed, steps):
+    """The indexer prolog on the query tokens of workload ``name``: timed like a step (L2 flushed before
     each), against HBM with its algorithmic bytes (bf16 q_proj, x and W_h read once; E4M3
     codes, per-head scales and fp32 weights written once)."""
-    inp = {k: v.to(dev) for k, v in W.prolog_inputs(cfg, seed).items()}
+    inp = {k: v.to(dev) for k, v in W.prolog_inputs(W.workload(name), seed).items()}
     T, h, d = inp["q_proj"].shape
     dm = inp["x"].shape[1]
     codes = torch.empty(T, h, d, dtype=torch.uint8, device=dev)
@@ -490,7 +495,8 @@ def prolog_record(dsa, W, torch, dist, dev, local, cfg, seed, steps):
             "workload": f"indexer prolog: T={T} tokens, H_I={h}, d_I={d}, d_model={dm}, bf16 in, "
                         f"E4M3 codes + per-token scale + fp32 head weights out",
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                         "traffic": measured_traffic("indexer_prolog", name),
                          "kernel": "indexer_prolog", "algorithmic_bytes_per_launch": alg,
                          "kernel_ms": kms, "peak_source": f"{src} hbm_gbs"},
             "clocks": clk, "gpu_launches": len(rec)}
