@@ -81,6 +81,10 @@ enum dsa_dtype {
 #define DSA_FLAG_BAD_INDEX 0x1u  /* SFA met an index outside [0, pos]; that entry was skipped */
 #define DSA_FLAG_BAD_SEQS  0x2u  /* cu_q/cu_k inconsistent with the descriptor; rows were skipped */
 #define DSA_FLAG_TIMEOUT   0x4u  /* a bounded on-device wait gave up; outputs are not valid */
+#define DSA_FLAG_CHECK     0x8u  /* checked build only (libdsa_checked.so, -DDSA_CHECKED): an
+                                  * internal invariant failed (a gather row outside the cache, a
+                                  * tile coordinate or query row out of range, an output slot at
+                                  * or past top_k); the access was clamped or skipped */
 
 /* Operations, for dsa_workspace_size(). */
 enum dsa_op {

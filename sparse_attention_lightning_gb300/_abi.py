@@ -1,16 +1,18 @@
 """ctypes declarations of libdsa.so (include/dsa.h).  Loading fails loudly."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa.so")
+CHECKED_LIB_PATH = os.path.join(_PKG, "libdsa_checked.so")  # -DDSA_CHECKED build
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_WORKSPACE, \
     DSA_ERR_TIMEOUT = range(6)
 DSA_F32, DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2, 3
-DSA_FLAG_BAD_INDEX, DSA_FLAG_BAD_SEQS, DSA_FLAG_TIMEOUT = 0x1, 0x2, 0x4
+DSA_FLAG_BAD_INDEX, DSA_FLAG_BAD_SEQS, DSA_FLAG_TIMEOUT, DSA_FLAG_CHECK = 0x1, 0x2, 0x4, 0x8
 OP_INDEXER_SCORES, OP_TOPK, OP_FUSED_INDEXER, OP_SPARSE_MLA_ATTN, OP_FUSED_FORWARD = 1, 2, 3, 4, 5
 
 # Every symbol include/dsa.h declares.
@@ -45,6 +47,20 @@ class DsaError(RuntimeError):
 
 
 _lib = None
+_path = LIB_PATH
+
+
+@contextlib.contextmanager
+def using(path: str):
+    """Route every call of the binding through the library at ``path`` (e.g. the checked
+    build) inside the ``with`` block."""
+    global _lib, _path
+    saved = (_lib, _path)
+    _lib, _path = None, path
+    try:
+        yield lib()
+    finally:
+        _lib, _path = saved
 
 
 def lib() -> ctypes.CDLL:
@@ -52,10 +68,10 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with "
+    if not os.path.exists(_path):
+        raise ImportError(f"{_path} is missing: build it with "
                           "`python -m sparse_attention_lightning_gb300.build`")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(_path)
     P = ctypes.POINTER(DsaProblem)
     vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
     sig = {
@@ -86,7 +102,7 @@ def lib() -> ctypes.CDLL:
     L.dsa_status_str.argtypes = [ctypes.c_int]
     L.dsa_last_error.argtypes = []
     if L.dsa_abi_version() != ABI_VERSION:
-        raise ImportError(f"{LIB_PATH} has ABI version {L.dsa_abi_version()}, the binding "
+        raise ImportError(f"{_path} has ABI version {L.dsa_abi_version()}, the binding "
                           f"expects {ABI_VERSION}: rebuild it")
     _lib = L
     return L

@@ -102,6 +102,20 @@ __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f32(__nv_fp8_e4m3 v) { return static_cast<float>(v); }
 
+// Checked builds (-DDSA_CHECKED, built as libdsa_checked.so): the kernels test their internal
+// invariants on the device (gather rows inside the cache, tile coordinates and query rows in
+// range, output slots below top_k).  A failed test sets DSA_FLAG_CHECK in the status word and
+// the caller clamps or skips the access; nothing traps.  Ordinary builds compile every test
+// away (dsa_check is constant true).
+#ifdef DSA_CHECKED
+__device__ __forceinline__ bool dsa_check(bool ok, uint32_t* status) {
+  if (!ok) atomicOr(status, DSA_FLAG_CHECK);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool dsa_check(bool, uint32_t*) { return true; }
+#endif
+
 // An E8M0 scale byte (the MX formats' shared scale) as fp32: 2^(e - 127).  e = 0 is the
 // fp32 subnormal 2^-127; e = 255 (NaN) is excluded by the interface.
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e) {

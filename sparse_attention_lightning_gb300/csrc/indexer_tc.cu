@@ -254,6 +254,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       for (int g = g0, it = 0; g < g1; ++g, ++it) {
         if (g > g0) cur.advance(tabs);
         if (g == g0 || cur.j == 0) {
+          dsa_check(cur.t >= 0 && cur.t < p.seqs.total_q, p.status);  // a query block inside q
           const int slot = blocks_seen % C::NQ;
           if (!mbar_wait(&q_empty[slot], ((blocks_seen / C::NQ) & 1) ^ 1, abort_flag, p.status,
                          DSA_FLAG_TIMEOUT)) break;
@@ -278,6 +279,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           mbar_arrive_expect_tx(&k_full[s], C::KTILE);
         }
         if (!p.seqs.paged()) {
+          dsa_check(key0 >= 0 && key0 < p.seqs.cache_rows(), p.status);  // the tile starts in the cache
           if (FP8) tma_load_2d(sdst, &smap, &k_full[s], key0 & ~3, 0);
           for (int a = 0; a < C::ATOMS; ++a)
             tma_load_2d_hint(ks + s * C::KTILE + a * (C::BM * 128), &kmap, &k_full[s],
@@ -474,7 +476,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const bool valid = r < cur.nrow && s <= cur.pos + r;
         float v = sum[rr];
         if (FP8 && !MX) v *= ksc;
-        if (valid) p.scores[(int64_t)(cur.t + r - p.r0) * p.ld + s] = v;
+        if (valid && dsa_check(cur.t + r - p.r0 >= 0 && cur.t + r < p.r1 && s < p.ld, p.status))
+          p.scores[(int64_t)(cur.t + r - p.r0) * p.ld + s] = v;
         if (p.hist) {
           // scores of neighbouring keys share bins: one shared-memory atomic per bin per warp
           if (valid) {

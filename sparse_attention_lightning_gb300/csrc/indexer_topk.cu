@@ -500,6 +500,7 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             ok = mbar_wait(&q_empty[qb], ((c >> 1) & 1) ^ 1, abort_flag, p.status, DSA_FLAG_TIMEOUT);
             if (!ok) break;
             mbar_arrive_expect_tx(&q_full[qb], C::QTILE);
+            dsa_check(runs[c].t >= 0 && runs[c].t < p.seqs.total_q, p.status);
             for (int a = 0; a < C::ATOMS; ++a)
               tma_load_2d(qs + qb * C::QTILE + a * (kHI * 128), &qmap, &q_full[qb],
                           a * (128 / C::ES), runs[c].t * kHI);
@@ -528,6 +529,7 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           float* sdst = scs + (it % NSCM) * (C::SC_SLOT / 4);
           if (!p.seqs.paged()) {
             const int key0 = r.k0 + s0;
+            dsa_check(key0 >= 0 && key0 < p.seqs.cache_rows(), p.status);
             if (FP8) tma_load_2d(sdst, &smap, &k_full[ss], key0 & ~3, 0);
             for (int a = 0; a < C::ATOMS; ++a)
               tma_load_2d_hint(kdst + a * (kBM * 128), &kmap, &k_full[ss], a * (128 / C::ES),
@@ -841,6 +843,7 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // every key of the history is kept: position s goes to slot s
       if (!failed)
         for (int j = tid; j < nkeys; j += kThreads) {
+          if (!dsa_check(s_lo + j < p.top_k, p.status)) break;
           irow[s_lo + j] = s_lo + j;
           if (vrow) vrow[s_lo + j] = sc[kb + j];
         }
@@ -1113,6 +1116,7 @@ indexer_topk_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           if (key > T) {
             slot = (int)(gb + min(eb, need));
             ++gb;
+            dsa_check(slot < k, p.status);  // every key above the threshold has a slot
           } else if (key == T) {
             if (eb < need) slot = (int)(gb + eb);
             ++eb;

@@ -378,9 +378,15 @@ sfa_tc_kernel(Params p) {
         }
         int cur[8], curh[4];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) cur[g] = rowid[g];
+        for (int g = 0; g < 8; ++g) {
+          cur[g] = rowid[g];
+          if (!dsa_check(cur[g] >= 0 && cur[g] < p.seqs.cache_rows(), p.status)) cur[g] = 0;
+        }
 #pragma unroll
-        for (int g = 0; g < 4; ++g) curh[g] = rowh[g];
+        for (int g = 0; g < 4; ++g) {
+          curh[g] = rowh[g];
+          if (!dsa_check(curh[g] >= 0 && curh[g] < p.seqs.cache_rows(), p.status)) curh[g] = 0;
+        }
         if (c + 1 < nch) load_rows(c + 1);
         const uint32_t dst0 = smem_u32(kvs + st * kKVStage);
         for (int a = 0; a < natoms; ++a) {
@@ -573,8 +579,9 @@ sfa_tc_kernel(Params p) {
       // The previous piece's logit MMAs are complete: both groups have passed the sum
       // exchange that ends it, after all of its chunks were staged.
       {
+        const int tq = dsa_check(t >= 0 && t < p.seqs.total_q, p.status) ? t : 0;
         const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + ((int64_t)t * kH + h) * kD + (rank ? kQK : 0) + 144 * grp);
+            p.q + ((int64_t)tq * kH + h) * kD + (rank ? kQK : 0) + 144 * grp);
         uint4 qv[18];
 #pragma unroll
         for (int i = 0; i < 18; ++i) qv[i] = __ldg(src + i);

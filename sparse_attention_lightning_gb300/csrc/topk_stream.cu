@@ -251,7 +251,8 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
     // only the (few) set bits: one iteration per selected key
     for (uint32_t m = dm; m; m &= m - 1u, ++pd) {
       const int j = __ffs(m) - 1;
-      if (pd < (uint32_t)k) {
+      // a definite key always has a slot (checked builds flag it; every build guards it)
+      if (dsa_check(pd < (uint32_t)k, a.status) && pd < (uint32_t)k) {
         irow[pd] = i0 + j;
         if (vrow) vrow[pd] = tl[j];
       }
@@ -330,7 +331,11 @@ __global__ void __launch_bounds__(kT, 2) topk_stream_kernel(TopkArgs a, int32_t*
   for (uint32_t c = c_lo; c < c_hi; ++c) {
     const uint2 ck = cand(c);
     int slot = -1;
-    if (ck.x > T) { slot = (int)(above + gb + min(eb, need)); ++gb; }
+    if (ck.x > T) {
+      slot = (int)(above + gb + min(eb, need));
+      ++gb;
+      dsa_check(slot < k, a.status);  // every candidate above the threshold has a slot
+    }
     else if (ck.x == T) { if (eb < need) slot = (int)(above + gb + eb); ++eb; }
     if (slot >= 0 && slot < k) {
       irow[slot] = (int32_t)ck.y;

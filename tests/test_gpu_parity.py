@@ -53,6 +53,12 @@ def check_rows(case, idx, vals, out, lse, rows):
         assert np.all(np.isneginf(vals_n[t, n:]))
         ref_out, ref_lse = p.sfa(t, sel)
         check_attn_row(out_n[t], lse_n[t], ref_out, ref_lse, tol, ctx)
+        # end to end: against the oracle's attention over its own Top-K set (positions
+        # swapped inside the tie band change the output by far less than the tolerance)
+        own = np.argsort(-I, kind="stable")[:n]
+        if not np.array_equal(np.sort(own), np.sort(sel)):
+            e2e_out, e2e_lse = p.sfa(t, own)
+            check_attn_row(out_n[t], lse_n[t], e2e_out, e2e_lse, tol, ctx + " (oracle's set)")
     return swaps
 
 
