@@ -283,7 +283,10 @@ sfa_tc_kernel(Params p) {
         // valid entries of the piece's slots of idx[t, :], in slot order -> list (absolute
         // key rows).  Each lane owns a contiguous run of up to 64 slots, loaded all at once
         // (independent loads).  The Top-K kernel that writes idx may still be running: wait
-        // for it here, after the work that does not depend on it.
+        // for it here, after the work that does not depend on it.  The loads are coherent
+        // (L2) ones: idx changes while this grid runs, so the read-only non-coherent path,
+        // which may be scheduled or cached as if the data were fixed for the whole launch,
+        // must not carry them.
         griddep_wait();
         const int slo = pc.a * kNC, shi = min(pc.b * kNC, p.top_k);
         const int32_t* irow = p.idx + (int64_t)t * p.top_k + slo;
@@ -293,7 +296,7 @@ sfa_tc_kernel(Params p) {
         int v[kMaxTopK / 32];
 #pragma unroll
         for (int j = 0; j < kMaxTopK / 32; ++j)
-          v[j] = (ok && j < seg && s0 + j < len) ? __ldg(irow + s0 + j) : -1;
+          v[j] = (ok && j < seg && s0 + j < len) ? __ldcg(irow + s0 + j) : -1;
         // valid entries: in [0, pos] (and, paged, on a page inside the cache; those become
         // their cache rows here, the others -1)
         int cnt = 0;
