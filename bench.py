@@ -42,21 +42,21 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     # (kernel, workload): (bytes per launch, sources, sha256 prefix of the sources); a kernel
     # whose sources changed since the capture reports null (profiles/ has the captures)
-    ("indexer_topk_bf16", "decode"): (179_346_944, ("indexer_topk.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "d9eb93a069b24d06"),
-    ("sfa_tc", "decode"): (83_959_808, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "b1b19e5969abc2a5"),
-    ("sfa_tc", "prefill_8k"): (2_323_838_976, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "b1b19e5969abc2a5"),
-    ("topk_stream", "prefill_8k"): (33_478_400, ("topk_stream.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "a77d9d9321f97c28"),
-    ("indexer_tc_bf16_qb4", "prefill_8k"): (58_037_248, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "51f180f72387c469"),
+    ("indexer_topk_bf16", "decode"): (179_720_960, ("indexer_topk.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "002b3bb0257570c9"),
+    ("sfa_tc", "decode"): (83_705_088, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "98834c9a4a2eadfe"),
+    ("sfa_tc", "prefill_8k"): (2_325_404_928, ("sfa_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "98834c9a4a2eadfe"),
+    ("topk_stream", "prefill_8k"): (33_431_040, ("topk_stream.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "5e134a9ae5e8b5fd"),
+    ("indexer_tc_bf16_qb4", "prefill_8k"): (57_766_912, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "25ff73549a3ca4b3"),
     # captured on the workload's first 16 of 128 sequences (--batch 16) and scaled by 8: the
     # key codes and their scales, read once, are 99 % of it and grow with the keys
-    ("indexer_tc_mxfp8", "mxfp8_decode"): (2_252_701_696, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
-                    "51f180f72387c469"),
-    ("indexer_prolog", "decode"): (1_932_800, ("prolog.cu", "dsa_internal.cuh"), "c6a5a8bce52afac8"),
+    ("indexer_tc_mxfp8", "mxfp8_decode"): (2_255_173_632, ("indexer_tc.cu", "tc_sm100.cuh", "dsa_internal.cuh"),
+                    "25ff73549a3ca4b3"),
+    ("indexer_prolog", "decode"): (1_932_800, ("prolog.cu", "dsa_internal.cuh"), "45d03705f2200f27"),
 }
 
 
