@@ -18,6 +18,17 @@ def test_check_flag_is_declared():
     assert "#define DSA_FLAG_CHECK     0x8u" in hdr and _abi.DSA_FLAG_CHECK == 0x8
 
 
+def test_checked_library_builds_and_exports_every_symbol():
+    # compiles for sm_103a without a GPU (about 20 s); nothing runs on a device
+    from sparse_attention_lightning_gb300 import build
+    assert build.build(checked=True) == _abi.CHECKED_LIB_PATH
+    with _abi.using(_abi.CHECKED_LIB_PATH) as L:
+        assert L.dsa_abi_version() == _abi.ABI_VERSION
+        for name in _abi.EXPORTS:
+            assert hasattr(L, name), name
+    assert _abi.lib()._name == _abi.LIB_PATH  # the ordinary library again outside the block
+
+
 CASES = [
     # (q_lens, k_lens, dims, idx dtype, page size): decode rows on the fused indexer (bf16,
     # FP8), several queries per sequence on the chunked indexer and streaming Top-K, MXFP8,
